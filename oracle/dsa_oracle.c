@@ -1,0 +1,337 @@
+/*
+ * CPU oracle for the DSA decode/prefill hot path (lightning indexer + Top-K + sparse flash attention).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load this library: only the tests, the
+ * package smoke check and the benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * constant with the CUDA library; its inputs come from the seeded generator and its arithmetic is
+ * written here from the definitions, in double precision, as plainly as possible.
+ *
+ * Sources (titles of the published articles the method is taken from):
+ *  [A1] "Optimizing Inference for Hybrid Attention LLMs: Practices for Fast Adaptation",
+ *       section 1 (sparse attention module bullet) and section 3.2 (index-gather-compute integration,
+ *       paged KV management).
+ *  [A2] "Optimizing Inference for Hybrid Attention Architectures: From Operator Fusion to Sequence
+ *       Sharding", section "Breaking Down the Computational Path of Hybrid Attention", steps 1
+ *       (index screening by the lightning indexer, head-importance weighting, Top-K) and 2 (sparse
+ *       flash attention over the selected KV).
+ *  [A3] "Day0 Inference Optimization for Next-Generation Hybrid-Architecture LLMs Based on CANN",
+ *       section 2.1 (fused scoring/weighting/Top-K reading the paged K cache) and section 3.1 (FP8
+ *       indexer inputs).
+ *  [A4] "Day0 Inference Support and Performance Optimization for New LLM Architectures", sections 3.1
+ *       (integrated indexer fusion: only Top-K indices leave the chip) and 3.2 (the sparse kernel
+ *       reads only the selected positions' KV from the paged cache).
+ *
+ * The articles describe the steps in prose and print no formula.  Readings used here:
+ *  - index score  I[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d])   (no softmax, no bias);
+ *  - FP8 inputs are E4M3 codes (OCP OFP8 definition) times one fp32 scale per row, applied literally;
+ *  - query t of sequence b (n_b new tokens, L_b cached tokens including them) sits at position
+ *    p = L_b - n_b + j and sees positions 0..p (causal, itself included);
+ *  - Top-K orders by score descending, then position ascending; with fewer than K visible positions
+ *    all are taken; the result is returned in ascending position order padded with -1;
+ *  - attention over the selected rows: z = scale * q . kv (all 576 dims), softmax over the selected
+ *    set, out = sum softmax * kv[:, :Dv] (V = leading Dv dims of the same latent row),
+ *    lse = max z + log sum exp(z - max z) (natural log).  No selected row: out = 0, lse = -inf.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int32_t batch;
+    int32_t total_q;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t max_pages_per_seq;
+    int32_t idx_heads;
+    int32_t idx_dim;
+    int32_t idx_fp8; /* 0: q_idx/k_idx are bf16 bits; 1: E4M3 codes with fp32 row scales */
+    int32_t top_k;
+    int32_t attn_heads;
+    int32_t kv_dim;
+    int32_t v_dim;
+    double softmax_scale;
+} oracle_dims;
+
+enum { ORC_OK = 0, ORC_BAD_ARG = -1, ORC_BAD_PAGE = -2, ORC_BAD_POS = -3, ORC_NOMEM = -4 };
+
+/* bf16 is the upper half of an IEEE binary32 value. */
+double oracle_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP OFP8 E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal
+ * (m/8 * 2^-6); S.1111.111 is NaN; there are no infinities. */
+double oracle_e4m3_value(uint8_t code) {
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Sequence of query token t and its causal position. */
+static int query_locate(const oracle_dims* d, const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t t,
+                        int32_t* b_out, int64_t* p_out) {
+    if (t < 0 || t >= d->total_q) return ORC_BAD_ARG;
+    for (int32_t b = 0; b < d->batch; ++b) {
+        if (t >= cu_q_lens[b] && t < cu_q_lens[b + 1]) {
+            int32_t n = cu_q_lens[b + 1] - cu_q_lens[b];
+            int32_t L = seq_lens[b];
+            if (n > L) return ORC_BAD_POS;
+            *b_out = b;
+            *p_out = (int64_t)L - n + (t - cu_q_lens[b]);
+            return ORC_OK;
+        }
+    }
+    return ORC_BAD_ARG;
+}
+
+/* Physical row of logical position s of sequence b ([A1] 3.2 paged KV management). */
+static int page_row(const oracle_dims* d, const int32_t* page_table, int32_t b, int64_t s, int64_t* row) {
+    int64_t lp = s / d->page_size;
+    if (lp >= d->max_pages_per_seq) return ORC_BAD_POS;
+    int32_t pg = page_table[(int64_t)b * d->max_pages_per_seq + lp];
+    if (pg < 0 || pg >= d->num_pages) return ORC_BAD_PAGE;
+    *row = (int64_t)pg * d->page_size + s % d->page_size;
+    return ORC_OK;
+}
+
+static double idx_elem(const oracle_dims* d, const void* base, const float* scales, int64_t row, int32_t col) {
+    if (d->idx_fp8) {
+        const uint8_t* p = (const uint8_t*)base;
+        return oracle_e4m3_value(p[row * d->idx_dim + col]) * (double)scales[row];
+    }
+    const uint16_t* p = (const uint16_t*)base;
+    return oracle_bf16_value(p[row * d->idx_dim + col]);
+}
+
+/*
+ * Index scores of query t against every visible position 0..p ([A2] step 1; [A3] 2.1):
+ * scores[s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d]).  Returns the count p+1 (>= 0) or an
+ * error code (< 0).  `scores` must hold at least p+1 values.
+ */
+int64_t oracle_index_scores(const oracle_dims* d, const void* q_idx, const float* q_scale, const float* w,
+                            const void* k_cache, const float* k_scale, const int32_t* page_table,
+                            const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t t, double* scores) {
+    int32_t b;
+    int64_t p;
+    int rc = query_locate(d, seq_lens, cu_q_lens, t, &b, &p);
+    if (rc) return rc;
+    const int32_t H = d->idx_heads, D = d->idx_dim;
+    double* q = (double*)malloc(sizeof(double) * (size_t)H * (size_t)D);
+    double* k = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!q || !k) {
+        free(q);
+        free(k);
+        return ORC_NOMEM;
+    }
+    for (int32_t h = 0; h < H; ++h)
+        for (int32_t j = 0; j < D; ++j)
+            q[h * D + j] = idx_elem(d, q_idx, q_scale, (int64_t)t * H + h, j);
+    for (int64_t s = 0; s <= p; ++s) {
+        int64_t row;
+        rc = page_row(d, page_table, b, s, &row);
+        if (rc) {
+            free(q);
+            free(k);
+            return rc;
+        }
+        for (int32_t j = 0; j < D; ++j) k[j] = idx_elem(d, k_cache, k_scale, row, j);
+        double I = 0.0;
+        for (int32_t h = 0; h < H; ++h) {
+            double dot = 0.0;
+            for (int32_t j = 0; j < D; ++j) dot += q[h * D + j] * k[j];
+            double relu = dot > 0.0 ? dot : 0.0;
+            I += (double)w[(int64_t)t * H + h] * relu;
+        }
+        scores[s] = I;
+    }
+    free(q);
+    free(k);
+    return p + 1;
+}
+
+typedef struct {
+    double score;
+    int64_t pos;
+} scored_pos;
+
+/* Score descending, then position ascending. */
+static int by_score_then_pos(const void* a, const void* b) {
+    const scored_pos* x = (const scored_pos*)a;
+    const scored_pos* y = (const scored_pos*)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+static int by_int32(const void* a, const void* b) {
+    int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Top-K selection for the listed query tokens ([A2] step 1; [A4] 3.1: only the Top-K indices are
+ * produced).  For each listed token i (global index tlist[i], or i itself when tlist is NULL):
+ *   topk[i*K .. i*K+K-1]  = selected positions, ascending, padded with -1;
+ *   kth[i]                = score of the last selected position in (score desc, pos asc) order;
+ *   nsel[i]               = min(K, p+1).
+ * Returns 0 or the first error code met.
+ */
+int oracle_indexer_topk(const oracle_dims* d, const void* q_idx, const float* q_scale, const float* w,
+                        const void* k_cache, const float* k_scale, const int32_t* page_table,
+                        const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* tlist, int32_t nt,
+                        int32_t* topk, double* kth, int32_t* nsel) {
+    int err = 0;
+    const int32_t K = d->top_k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t i = 0; i < nt; ++i) {
+        int32_t t = tlist ? tlist[i] : i;
+        int32_t b;
+        int64_t p;
+        int rc = query_locate(d, seq_lens, cu_q_lens, t, &b, &p);
+        int32_t* out = topk + (int64_t)i * K;
+        for (int32_t k = 0; k < K; ++k) out[k] = -1;
+        if (rc) {
+#pragma omp atomic write
+            err = rc;
+            continue;
+        }
+        int64_t n = p + 1;
+        double* sc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        scored_pos* sp = (scored_pos*)malloc(sizeof(scored_pos) * (size_t)(n > 0 ? n : 1));
+        if (!sc || !sp) {
+            free(sc);
+            free(sp);
+#pragma omp atomic write
+            err = ORC_NOMEM;
+            continue;
+        }
+        int64_t got = oracle_index_scores(d, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens,
+                                          cu_q_lens, t, sc);
+        if (got < 0) {
+            free(sc);
+            free(sp);
+#pragma omp atomic write
+            err = (int)got;
+            continue;
+        }
+        for (int64_t s = 0; s < n; ++s) {
+            sp[s].score = sc[s] == 0.0 ? 0.0 : sc[s]; /* -0.0 ranks as +0.0 */
+            sp[s].pos = s;
+        }
+        qsort(sp, (size_t)n, sizeof(scored_pos), by_score_then_pos);
+        int32_t m = (int32_t)(n < K ? n : K);
+        for (int32_t k = 0; k < m; ++k) out[k] = (int32_t)sp[k].pos;
+        qsort(out, (size_t)m, sizeof(int32_t), by_int32);
+        if (kth) kth[i] = m > 0 ? sp[m - 1].score : -INFINITY;
+        if (nsel) nsel[i] = m;
+        free(sc);
+        free(sp);
+    }
+    return err;
+}
+
+/*
+ * Sparse flash attention over the selected rows ([A2] step 2; [A4] 3.2; [A1] 3.2 gather):
+ * for each listed token i and head h, with S = {topk[i, k] >= 0}:
+ *   z_s = scale * sum_{c < kv_dim} q[t,h,c] * kv[s,c]
+ *   out[i,h,:] = sum_s softmax(z)_s * kv[s, :v_dim],  lse[i,h] = logsumexp(z).
+ * topk rows are indexed by list position i (row i belongs to token tlist[i]).
+ * weights (optional, [nt, H, K]) receives softmax(z) in topk order (0 for -1 entries).
+ */
+int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const uint16_t* kv_cache,
+                       const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                       const int32_t* topk, const int32_t* tlist, int32_t nt, double* out, double* lse,
+                       double* weights) {
+    int err = 0;
+    const int32_t H = d->attn_heads, C = d->kv_dim, V = d->v_dim, K = d->top_k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t i = 0; i < nt; ++i) {
+        int32_t t = tlist ? tlist[i] : i;
+        int32_t b;
+        int64_t p;
+        int rc = query_locate(d, seq_lens, cu_q_lens, t, &b, &p);
+        if (rc) {
+#pragma omp atomic write
+            err = rc;
+            continue;
+        }
+        const int32_t* sel = topk + (int64_t)i * K;
+        int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(K > 0 ? K : 1));
+        double* z = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!rows || !z) {
+            free(rows);
+            free(z);
+#pragma omp atomic write
+            err = ORC_NOMEM;
+            continue;
+        }
+        int bad = 0;
+        for (int32_t k = 0; k < K; ++k) {
+            rows[k] = -1;
+            if (sel[k] < 0) continue;
+            if (sel[k] > p) {
+                bad = ORC_BAD_POS;
+                break;
+            }
+            if (page_row(d, page_table, b, sel[k], &rows[k])) {
+                bad = ORC_BAD_PAGE;
+                break;
+            }
+        }
+        if (bad) {
+            free(rows);
+            free(z);
+#pragma omp atomic write
+            err = bad;
+            continue;
+        }
+        for (int32_t h = 0; h < H; ++h) {
+            const uint16_t* qh = q + ((int64_t)t * H + h) * C;
+            double zmax = -INFINITY;
+            int32_t count = 0;
+            for (int32_t k = 0; k < K; ++k) {
+                if (rows[k] < 0) continue;
+                const uint16_t* r = kv_cache + rows[k] * C;
+                double dot = 0.0;
+                for (int32_t c = 0; c < C; ++c) dot += oracle_bf16_value(qh[c]) * oracle_bf16_value(r[c]);
+                z[k] = d->softmax_scale * dot;
+                if (z[k] > zmax) zmax = z[k];
+                ++count;
+            }
+            double* o = out + ((int64_t)i * H + h) * V;
+            for (int32_t v = 0; v < V; ++v) o[v] = 0.0;
+            double* wrow = weights ? weights + ((int64_t)i * H + h) * K : NULL;
+            if (wrow)
+                for (int32_t k = 0; k < K; ++k) wrow[k] = 0.0;
+            if (count == 0) {
+                lse[(int64_t)i * H + h] = -INFINITY;
+                continue;
+            }
+            double denom = 0.0;
+            for (int32_t k = 0; k < K; ++k)
+                if (rows[k] >= 0) denom += exp(z[k] - zmax);
+            for (int32_t k = 0; k < K; ++k) {
+                if (rows[k] < 0) continue;
+                double a = exp(z[k] - zmax) / denom;
+                if (wrow) wrow[k] = a;
+                const uint16_t* r = kv_cache + rows[k] * C;
+                for (int32_t v = 0; v < V; ++v) o[v] += a * oracle_bf16_value(r[v]);
+            }
+            lse[(int64_t)i * H + h] = zmax + log(denom);
+        }
+        free(rows);
+        free(z);
+    }
+    return err;
+}
