@@ -1,0 +1,168 @@
+/*
+ * dsa.h - C ABI of the GB300 (sm_103a) library for the DSA decode/prefill hot path:
+ * a fused lightning indexer with on-chip Top-K selection, followed by sparse flash attention (SFA)
+ * over the selected rows of a paged MLA latent-KV cache.
+ *
+ * The operations follow these published articles (cited by title and section):
+ *  [A1] "Optimizing Inference for Hybrid Attention LLMs: Practices for Fast Adaptation", sections 1 and
+ *       3.2 (index-gather-compute integration; paged KV management; gather/compute overlap).
+ *  [A2] "Optimizing Inference for Hybrid Attention Architectures: From Operator Fusion to Sequence
+ *       Sharding", section "Breaking Down the Computational Path of Hybrid Attention" (steps 1 and 2) and
+ *       section "Fusing Index Screening with Multi-Stream Orchestration".
+ *  [A3] "Day0 Inference Optimization for Next-Generation Hybrid-Architecture LLMs Based on CANN",
+ *       sections 2.1 (deep operator fusion) and 3.1 (FP8 indexer inputs).
+ *  [A4] "Day0 Inference Support and Performance Optimization for New LLM Architectures", sections 3.1
+ *       (integrated indexer fusion) and 3.2 (sparse attention kernel).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller owns every buffer.  All array arguments are DEVICE pointers (memory of the
+ *    current CUDA device) unless stated otherwise; `dims` is a host pointer read during the call only.
+ *    The library keeps no state between calls and allocates no device memory.
+ *  - Execution: compute calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise with the host, so they can be captured in a CUDA graph.
+ *  - Errors: argument problems are detected on the host and returned synchronously before any launch
+ *    (DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED; dsa_last_error_message() explains).  Problems found on
+ *    the device (an out-of-range page id, inconsistent lengths, a bounded wait that gave up) set bits in
+ *    the workspace error word; the kernels skip the affected work and return normally.  Read the word
+ *    with dsa_get_device_error().  A failed launch returns DSA_ERR_CUDA.
+ *  - Layout: tensors are dense and row-major in the shapes given below; every array pointer must be
+ *    16-byte aligned.
+ *  - Paging ([A1] 3.2): logical position s of sequence b lives in row s % page_size of physical page
+ *    page_table[b * max_pages_per_seq + s / page_size].  The indexer K cache and the latent-KV cache
+ *    share one page table.  page_size must be 64.
+ *  - Queries: sequence b owns query tokens cu_q_lens[b] .. cu_q_lens[b+1]-1 (n_b of them).
+ *    seq_lens[b] = L_b counts the cached tokens INCLUDING those n_b new ones, so query j of sequence b
+ *    sits at position p = L_b - n_b + j and sees positions 0..p (causal, itself included).
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, a negative or inconsistent size */
+    DSA_ERR_UNSUPPORTED = 2, /* valid arguments outside what this build implements (see each call) */
+    DSA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    DSA_ERR_DEVICE = 4,      /* dsa_get_device_error(): the device error word is non-zero */
+    DSA_ERR_TIMEOUT = 5      /* dsa_get_device_error(): a bounded device wait gave up */
+} dsa_status_t;
+
+typedef enum {
+    DSA_BF16 = 0,     /* bfloat16 */
+    DSA_FP8_E4M3 = 1  /* OCP OFP8 E4M3 codes, each row with one fp32 scale ([A3] 3.1) */
+} dsa_dtype_t;
+
+/* Bits of the device error word (the first int32 of the workspace). */
+#define DSA_DEVERR_PAGE 0x1    /* a page-table entry outside [0, num_pages) was needed */
+#define DSA_DEVERR_SEQ 0x2     /* n_b > L_b, or L_b > max_pages_per_seq * page_size */
+#define DSA_DEVERR_INDEX 0x4   /* a Top-K entry outside [-1, p] reached the attention kernel */
+#define DSA_DEVERR_TIMEOUT 0x8 /* a pipeline wait exceeded its limit (about one second) */
+
+typedef struct {
+    int32_t batch;             /* B >= 1 sequences */
+    int32_t total_q;           /* T = cu_q_lens[B] query tokens (0 allowed: nothing to do) */
+    int32_t max_q_len;         /* >= max_b n_b, >= 1 */
+    int32_t num_pages;         /* physical pages in each cache */
+    int32_t page_size;         /* tokens per page; must be 64 */
+    int32_t max_pages_per_seq; /* row length of page_table */
+    int32_t idx_heads;         /* Hi, indexer heads */
+    int32_t idx_dim;           /* Di, indexer head dim */
+    int32_t idx_dtype;         /* dsa_dtype_t of q_idx and the indexer K cache */
+    int32_t top_k;             /* K, positions kept per query */
+    int32_t attn_heads;        /* Hq, attention heads sharing the latent KV rows */
+    int32_t kv_dim;            /* D, latent KV row width (512 latent + 64 RoPE = 576) */
+    int32_t v_dim;             /* Dv, leading dims of each row used as V (512) */
+    float softmax_scale;       /* multiplies q . kv before the softmax (1/sqrt(576)) */
+} dsa_dims_t;
+
+/* ABI version of the loaded library (DSA_ABI_VERSION). */
+int32_t dsa_abi_version(void);
+
+/* Static description of a status code. */
+const char* dsa_status_string(dsa_status_t status);
+
+/* Human-readable reason for the last non-OK status returned on this host thread ("" if none). */
+const char* dsa_last_error_message(void);
+
+/*
+ * Bytes of device workspace the compute calls need for `dims` (at least 256: the error word plus
+ * padding).  The caller allocates it once, zero-fills it before first use, and passes the same
+ * buffer to later calls; the error word latches until dsa_clear_device_error().  Returns 0 when dims
+ * is NULL.  Calls that may overlap on the GPU need separate workspaces.
+ */
+size_t dsa_workspace_size(const dsa_dims_t* dims);
+
+/*
+ * Lightning indexer + Top-K ([A2] step 1; [A3] 2.1; [A4] 3.1): for every query token t,
+ *     I[t,s] = sum_h w[t,h] * max(0, q_idx[t,h,:] . k[s,:])      for s = 0..p_t,
+ * and keep the K positions with the largest I (ties: the lower position wins).  The scores stay on
+ * chip; only the selected positions are written.  With FP8 inputs, q_idx[t,h,:] and k[s,:] are the
+ * codes times their row scales.
+ *   q_idx        [T, Hi, Di]  bf16, or E4M3 codes (uint8) when dims->idx_dtype == DSA_FP8_E4M3
+ *   q_scale      [T, Hi]      fp32 row scales of q_idx (FP8 only; NULL for bf16)
+ *   w            [T, Hi]      fp32 head weights
+ *   k_cache      [num_pages, 64, Di]  paged indexer keys, same dtype as q_idx
+ *   k_scale      [num_pages, 64]      fp32 row scales of k_cache (FP8 only; NULL for bf16)
+ *   page_table   [B, max_pages_per_seq] int32;  seq_lens [B] int32;  cu_q_lens [B+1] int32
+ *   topk_idx     [T, K] int32 output: the selected positions of each query in ascending order; when
+ *                fewer than K positions are visible all of them are kept and the rest is -1.
+ *   workspace    dsa_workspace_size(dims) bytes (see above)
+ * Supported: (Hi, Di) = (4, 64) or (64, 128) in bf16, (64, 128) in FP8; K <= 4096; per sequence at
+ * most 2 query tokens when max_pages_per_seq * 64 > 65536, else at most 4 (DSA_ERR_UNSUPPORTED
+ * otherwise).
+ */
+dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
+                              const void* k_cache, const float* k_scale, const int32_t* page_table,
+                              const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx,
+                              void* workspace, void* stream);
+
+/*
+ * Sparse flash attention over the selected rows ([A2] step 2; [A4] 3.2; [A1] 3.2): for every query
+ * token t and head h, with S_t = { topk_idx[t,k] : topk_idx[t,k] >= 0 } (any order; -1 entries are
+ * skipped),
+ *     z_s = softmax_scale * q[t,h,:] . kv[s,:]           (all kv_dim dims)
+ *     out[t,h,:] = sum_{s in S_t} softmax(z)_s * kv[s, 0:v_dim]
+ *     lse[t,h]   = log sum_{s in S_t} exp(z_s)           (natural log; -inf and out = 0 if S_t is empty)
+ *   q          [T, Hq, D] bf16;  kv_cache [num_pages, 64, D] bf16 (V = the first Dv dims of each row)
+ *   topk_idx   [T, K] int32 logical positions (entries outside [-1, p_t] set DSA_DEVERR_INDEX and are
+ *              skipped)
+ *   out        [T, Hq, Dv] bf16 output;  lse [T, Hq] fp32 output (may be NULL)
+ * Supported: D = 576, Dv = 512, Hq <= 128, K <= 4096.
+ */
+dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* kv_cache, const int32_t* page_table,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out,
+                             float* lse, void* workspace, void* stream);
+
+/*
+ * The whole decode/prefill step: dsa_indexer_topk followed by dsa_sparse_attn on the same stream
+ * ([A2] "Fusing Index Screening with Multi-Stream Orchestration"; [A4] 3.1-3.2).  topk_idx is an
+ * output (the selection used by the attention).  Arguments and limits are those of the two calls.
+ */
+dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
+                              const void* k_cache, const float* k_scale, const void* q, const void* kv_cache,
+                              const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                              int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream);
+
+/*
+ * Synchronises `stream`, then reads the device error word of `workspace` into *code (host pointer).
+ * Returns DSA_OK if it is zero, DSA_ERR_TIMEOUT if DSA_DEVERR_TIMEOUT is set, DSA_ERR_DEVICE for any
+ * other bit, DSA_ERR_CUDA if the synchronisation or the copy fails.
+ */
+dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* code);
+
+/* Zeroes the device error word (asynchronously on `stream`). */
+dsa_status_t dsa_clear_device_error(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

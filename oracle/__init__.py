@@ -76,6 +76,8 @@ def lib():
             L.oracle_index_scores.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 8 + [i32, vp]
             L.oracle_indexer_topk.restype = ctypes.c_int
             L.oracle_indexer_topk.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 9 + [i32, vp, vp, vp]
+            L.oracle_index_scores_batch.restype = ctypes.c_int
+            L.oracle_index_scores_batch.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 9 + [i32, ctypes.c_int64, vp]
             L.oracle_sparse_attn.restype = ctypes.c_int
             L.oracle_sparse_attn.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 7 + [i32, vp, vp, vp]
             _lib = L
@@ -125,6 +127,19 @@ def index_scores(wl, t: int) -> np.ndarray:
                                    _p(out))
     _check(rc)
     return out[: pos + 1]
+
+
+def index_scores_batch(wl, tlist):
+    """List of float64 score arrays I[t, 0..p_t] for the tokens in tlist (computed in parallel)."""
+    tl = np.ascontiguousarray(tlist, dtype=np.int32)
+    pos = wl.query_positions()[tl]
+    stride = int(pos.max()) + 1 if len(tl) else 1
+    buf = np.empty((len(tl), stride), dtype=np.float64)
+    rc = lib().oracle_index_scores_batch(ctypes.byref(_dims(wl)), _p(wl.q_idx), _p(wl.q_scale), _p(wl.w),
+                                         _p(wl.k_cache), _p(wl.k_scale), _p(wl.page_table), _p(wl.seq_lens),
+                                         _p(wl.cu_q_lens), _p(tl), len(tl), stride, _p(buf))
+    _check(rc)
+    return [buf[i, : int(pos[i]) + 1] for i in range(len(tl))]
 
 
 def indexer_topk(wl, tlist=None):

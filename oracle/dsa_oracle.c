@@ -335,3 +335,25 @@ int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const uint16_t* 
     }
     return err;
 }
+
+/*
+ * Index scores of several query tokens at once (OpenMP over the list): row i of `scores` (stride
+ * `stride` values) receives I[tlist[i], 0..p], the rest of the row is left untouched.  Returns 0 or
+ * the first error code met.
+ */
+int oracle_index_scores_batch(const oracle_dims* d, const void* q_idx, const float* q_scale, const float* w,
+                              const void* k_cache, const float* k_scale, const int32_t* page_table,
+                              const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* tlist, int32_t nt,
+                              int64_t stride, double* scores) {
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t i = 0; i < nt; ++i) {
+        int64_t got = oracle_index_scores(d, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens,
+                                          tlist[i], scores + (int64_t)i * stride);
+        if (got < 0) {
+#pragma omp atomic write
+            err = (int)got;
+        }
+    }
+    return err;
+}

@@ -1,0 +1,359 @@
+// C ABI (include/dsa.h): argument validation, work planning, tensor-map encoding and kernel launches.
+// No device memory is allocated here and nothing synchronises with the host except
+// dsa_get_device_error().
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "dsa.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+dsa_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(DSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+    int num_sms = 0;
+    int smem_optin = 0;
+};
+
+dsa_status_t device_info(DeviceInfo* out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!have[dev]) {
+        DeviceInfo d;
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(DSA_ERR_UNSUPPORTED, "this library is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = cache[dev];
+    return DSA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dsa_status_t check_ptr(const void* p, const char* name, bool required = true) {
+    if (!p) return required ? fail(DSA_ERR_INVALID_ARG, "%s is NULL", name) : DSA_OK;
+    if (!aligned16(p)) return fail(DSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return DSA_OK;
+}
+
+dsa_status_t check_common(const dsa_dims_t* d) {
+    if (!d) return fail(DSA_ERR_INVALID_ARG, "dims is NULL");
+    if (d->batch < 1) return fail(DSA_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", d->batch);
+    if (d->total_q < 0) return fail(DSA_ERR_INVALID_ARG, "total_q must be >= 0 (got %d)", d->total_q);
+    if (d->max_q_len < 1) return fail(DSA_ERR_INVALID_ARG, "max_q_len must be >= 1 (got %d)", d->max_q_len);
+    if (d->num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "num_pages must be >= 1 (got %d)", d->num_pages);
+    if (d->page_size < 1) return fail(DSA_ERR_INVALID_ARG, "page_size must be >= 1 (got %d)", d->page_size);
+    if (d->page_size != 64) return fail(DSA_ERR_UNSUPPORTED, "page_size must be 64 (got %d)", d->page_size);
+    if (d->max_pages_per_seq < 1)
+        return fail(DSA_ERR_INVALID_ARG, "max_pages_per_seq must be >= 1 (got %d)", d->max_pages_per_seq);
+    if ((int64_t)d->max_pages_per_seq * 64 > (int64_t)INT32_MAX)
+        return fail(DSA_ERR_UNSUPPORTED, "max_pages_per_seq * 64 exceeds int32");
+    if (d->top_k < 1) return fail(DSA_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", d->top_k);
+    if (d->top_k > 16384) return fail(DSA_ERR_UNSUPPORTED, "top_k must be <= 16384 (got %d)", d->top_k);
+    return DSA_OK;
+}
+
+constexpr int kKeyBudgetBytes = 64 * 1024;
+
+dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::IndexerLaunch* L) {
+    if (d->idx_heads < 1 || d->idx_dim < 1)
+        return fail(DSA_ERR_INVALID_ARG, "idx_heads and idx_dim must be >= 1 (got %d, %d)", d->idx_heads, d->idx_dim);
+    if (d->idx_dtype != DSA_BF16 && d->idx_dtype != DSA_FP8_E4M3)
+        return fail(DSA_ERR_INVALID_ARG, "idx_dtype %d is not a dsa_dtype_t", d->idx_dtype);
+    const bool fp8 = d->idx_dtype == DSA_FP8_E4M3;
+    const int64_t max_ctx = (int64_t)d->max_pages_per_seq * 64;
+    int qb_max;
+    if (!fp8 && d->idx_heads == 4 && d->idx_dim == 64)
+        qb_max = 4;
+    else if (d->idx_heads == 64 && d->idx_dim == 128)
+        qb_max = (!fp8 && max_ctx <= 65536) ? 4 : 2;
+    else
+        return fail(DSA_ERR_UNSUPPORTED, "indexer shape (heads %d, dim %d, %s) has no kernel variant", d->idx_heads,
+                    d->idx_dim, fp8 ? "fp8" : "bf16");
+    int qb = d->max_q_len < qb_max ? d->max_q_len : qb_max;
+    if (qb == 3) qb = 4;
+    const int qb_template = (d->idx_heads == 4) ? 4 : qb;  // the Hi=4 variant always reserves 4 query slots
+    if (dsa::indexer_variant_n(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, qb) == 0)
+        return fail(DSA_ERR_UNSUPPORTED, "no indexer variant for %d query tokens per block", qb);
+    const int blocks_per_seq = (d->max_q_len + qb - 1) / qb;
+    const int64_t items = (int64_t)d->batch * blocks_per_seq;
+    if (items > (1 << 26)) return fail(DSA_ERR_UNSUPPORTED, "too many work items (%lld)", (long long)items);
+    auto chunk_for = [&](int C) -> int64_t {
+        const int64_t per = (max_ctx + C - 1) / C;
+        return (per + 127) / 128 * 128;
+    };
+    int c_min = 0;
+    for (int C = 1; C <= 16; C *= 2)
+        if (chunk_for(C) * qb_template * 4 <= kKeyBudgetBytes) {
+            c_min = C;
+            break;
+        }
+    if (c_min == 0)
+        return fail(DSA_ERR_UNSUPPORTED, "context of %lld positions with %d query tokens per block exceeds the on-chip "
+                    "score capacity (16 CTAs x %d KiB)", (long long)max_ctx, qb, kKeyBudgetBytes / 1024);
+    int c_target = 1;
+    while (c_target < 16 && items * (c_target * 2) <= dev.num_sms) c_target *= 2;
+    const int C = c_min > c_target ? c_min : c_target;
+    L->cluster = C;
+    L->items = (int)items;
+    L->idx_heads = d->idx_heads;
+    L->idx_dim = d->idx_dim;
+    L->fp8 = fp8;
+    L->smem_limit = dev.smem_optin;
+    L->check_occupancy = true;
+    dsa::IndexerParams& p = L->params;
+    memset(&p, 0, sizeof p);
+    p.batch = d->batch;
+    p.total_q = d->total_q;
+    p.num_pages = d->num_pages;
+    p.max_pages = d->max_pages_per_seq;
+    p.top_k = d->top_k;
+    p.qb = qb;
+    p.blocks_per_seq = blocks_per_seq;
+    p.chunk = (int)chunk_for(C);
+    return DSA_OK;
+}
+
+dsa_status_t encode_indexer_maps(const dsa_dims_t* d, const void* q_idx, const void* k_cache, int n_cols,
+                                 dsa::IndexerLaunch* L) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const bool fp8 = L->fp8;
+    const int elem = fp8 ? 1 : 2;
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint32_t inner_box = (cuuint32_t)(128 / elem);
+    {
+        const cuuint64_t gdim[3] = {(cuuint64_t)d->idx_dim, 64, (cuuint64_t)d->num_pages};
+        const cuuint64_t gstride[2] = {(cuuint64_t)d->idx_dim * elem, (cuuint64_t)64 * d->idx_dim * elem};
+        const cuuint32_t box[3] = {inner_box, 64, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        CUresult r = enc(&L->kmap, dt, 3, const_cast<void*>(k_cache), gdim, gstride, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "tensor map for k_cache: CUresult %d", (int)r);
+    }
+    {
+        const cuuint64_t gdim[2] = {(cuuint64_t)d->idx_dim, (cuuint64_t)d->total_q * d->idx_heads};
+        const cuuint64_t gstride[1] = {(cuuint64_t)d->idx_dim * elem};
+        const cuuint32_t box[2] = {inner_box, (cuuint32_t)n_cols};
+        const cuuint32_t es[2] = {1, 1};
+        CUresult r = enc(&L->qmap, dt, 2, const_cast<void*>(q_idx), gdim, gstride, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "tensor map for q_idx: CUresult %d", (int)r);
+    }
+    return DSA_OK;
+}
+
+dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_scale, const float* w,
+                         const void* k_cache, const float* k_scale, const int32_t* page_table, const int32_t* seq_lens,
+                         const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace, void* stream) {
+    dsa_status_t st = check_common(d);
+    if (st) return st;
+    const bool fp8 = d->idx_dtype == DSA_FP8_E4M3;
+    if ((st = check_ptr(q_idx, "q_idx")) || (st = check_ptr(w, "w")) || (st = check_ptr(k_cache, "k_cache")) ||
+        (st = check_ptr(page_table, "page_table")) || (st = check_ptr(seq_lens, "seq_lens")) ||
+        (st = check_ptr(cu_q_lens, "cu_q_lens")) || (st = check_ptr(topk_idx, "topk_idx")) ||
+        (st = check_ptr(workspace, "workspace")))
+        return st;
+    if (fp8 && ((st = check_ptr(q_scale, "q_scale")) || (st = check_ptr(k_scale, "k_scale")))) return st;
+    DeviceInfo dev;
+    if ((st = device_info(&dev))) return st;
+    dsa::IndexerLaunch L;
+    memset(&L, 0, sizeof L);
+    if ((st = plan_indexer(d, dev, &L))) return st;
+    if (d->total_q == 0) return DSA_OK;
+    const int n_cols = dsa::indexer_variant_n(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, L.params.qb);
+    if ((st = encode_indexer_maps(d, q_idx, k_cache, n_cols, &L))) return st;
+    dsa::IndexerParams& p = L.params;
+    p.q_scale = fp8 ? q_scale : nullptr;
+    p.w = w;
+    p.k_scale = fp8 ? k_scale : nullptr;
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.cu_q_lens = cu_q_lens;
+    p.topk = topk_idx;
+    p.err = static_cast<int32_t*>(workspace);
+    cudaError_t e = dsa::launch_indexer(L, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidClusterSize)
+        return fail(DSA_ERR_UNSUPPORTED, "a cluster of %d CTAs does not fit on this device", L.cluster);
+    if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+    return DSA_OK;
+}
+
+dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
+                     const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out, float* lse,
+                     void* workspace, void* stream) {
+    dsa_status_t st = check_common(d);
+    if (st) return st;
+    if (d->attn_heads < 1) return fail(DSA_ERR_INVALID_ARG, "attn_heads must be >= 1 (got %d)", d->attn_heads);
+    if (d->kv_dim < 1 || d->v_dim < 1 || d->v_dim > d->kv_dim)
+        return fail(DSA_ERR_INVALID_ARG, "need 1 <= v_dim <= kv_dim (got %d, %d)", d->v_dim, d->kv_dim);
+    if (d->kv_dim != 576 || d->v_dim != 512)
+        return fail(DSA_ERR_UNSUPPORTED, "sparse attention supports kv_dim 576 / v_dim 512 (got %d / %d)", d->kv_dim,
+                    d->v_dim);
+    if (d->attn_heads > 128) return fail(DSA_ERR_UNSUPPORTED, "attn_heads must be <= 128 (got %d)", d->attn_heads);
+    if (!(d->softmax_scale > 0.f) || d->softmax_scale > 1e30f)
+        return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be a positive finite number");
+    if ((st = check_ptr(q, "q")) || (st = check_ptr(kv_cache, "kv_cache")) ||
+        (st = check_ptr(page_table, "page_table")) || (st = check_ptr(seq_lens, "seq_lens")) ||
+        (st = check_ptr(cu_q_lens, "cu_q_lens")) || (st = check_ptr(topk_idx, "topk_idx")) ||
+        (st = check_ptr(out, "out")) || (st = check_ptr(lse, "lse", false)) ||
+        (st = check_ptr(workspace, "workspace")))
+        return st;
+    DeviceInfo dev;
+    if ((st = device_info(&dev))) return st;
+    if (d->total_q == 0) return DSA_OK;
+    dsa::SfaLaunch L;
+    memset(&L, 0, sizeof L);
+    dsa::SfaParams& p = L.params;
+    p.q = static_cast<const uint16_t*>(q);
+    p.kv_cache = static_cast<const uint16_t*>(kv_cache);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.cu_q_lens = cu_q_lens;
+    p.topk = topk_idx;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.err = static_cast<int32_t*>(workspace);
+    p.batch = d->batch;
+    p.total_q = d->total_q;
+    p.num_pages = d->num_pages;
+    p.max_pages = d->max_pages_per_seq;
+    p.top_k = d->top_k;
+    p.heads = d->attn_heads;
+    p.kv_dim = d->kv_dim;
+    p.v_dim = d->v_dim;
+    p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
+    L.smem_limit = dev.smem_optin;
+    L.num_sms = dev.num_sms;
+    cudaError_t e = dsa::launch_sfa(L, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_status_string(dsa_status_t s) {
+    switch (s) {
+        case DSA_OK: return "DSA_OK";
+        case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG: invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: valid arguments this build does not implement";
+        case DSA_ERR_CUDA: return "DSA_ERR_CUDA: a CUDA call failed";
+        case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE: the device error word is set";
+        case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "unknown dsa_status_t";
+}
+
+const char* dsa_last_error_message(void) { return g_last_error.c_str(); }
+
+size_t dsa_workspace_size(const dsa_dims_t* dims) { return dims ? 256 : 0; }
+
+dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
+                              const void* k_cache, const float* k_scale, const int32_t* page_table,
+                              const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace,
+                              void* stream) {
+    g_last_error.clear();
+    return run_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx, workspace,
+                       stream);
+}
+
+dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* kv_cache, const int32_t* page_table,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out,
+                             float* lse, void* workspace, void* stream) {
+    g_last_error.clear();
+    return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream);
+}
+
+dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
+                              const void* k_cache, const float* k_scale, const void* q, const void* kv_cache,
+                              const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                              int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream) {
+    g_last_error.clear();
+    dsa_status_t st = run_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx,
+                                  workspace, stream);
+    if (st) return st;
+    return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream);
+}
+
+dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* code) {
+    g_last_error.clear();
+    if (!workspace || !code) return fail(DSA_ERR_INVALID_ARG, "workspace and code must be non-NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    *code = v;
+    if (v == 0) return DSA_OK;
+    if (v & DSA_DEVERR_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "device error word 0x%x", v);
+    return fail(DSA_ERR_DEVICE, "device error word 0x%x", v);
+}
+
+dsa_status_t dsa_clear_device_error(void* workspace, void* stream) {
+    g_last_error.clear();
+    if (!workspace) return fail(DSA_ERR_INVALID_ARG, "workspace is NULL");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    return DSA_OK;
+}
+
+}  // extern "C"

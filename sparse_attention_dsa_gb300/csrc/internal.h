@@ -1,0 +1,81 @@
+// Launch descriptions shared between the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+constexpr int kMaxStages = 8;
+
+// ---- lightning indexer + Top-K -----------------------------------------------------------------------
+struct IndexerParams {
+    const float* q_scale;  // [T, Hi] (FP8 only)
+    const float* w;        // [T, Hi]
+    const float* k_scale;  // [num_pages, 64] (FP8 only)
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const int32_t* cu_q_lens;
+    int32_t* topk;  // [T, K]
+    int32_t* err;   // device error word
+    int32_t batch;
+    int32_t total_q;
+    int32_t num_pages;
+    int32_t max_pages;
+    int32_t top_k;
+    int32_t qb;              // query tokens per cluster work item
+    int32_t blocks_per_seq;  // ceil(max_q_len / qb)
+    int32_t chunk;           // positions per CTA (multiple of 128)
+    int32_t stages;          // filled in by the launcher
+};
+
+struct IndexerLaunch {
+    CUtensorMap kmap;  // 3-D view [num_pages][64][Di] of the indexer K cache
+    CUtensorMap qmap;  // 2-D view [T*Hi][Di] of q_idx
+    IndexerParams params;
+    int items;    // work items (clusters)
+    int cluster;  // CTAs per cluster
+    int idx_heads;
+    int idx_dim;
+    bool fp8;
+    int smem_limit;  // opt-in dynamic shared memory per block
+    bool check_occupancy;
+};
+
+// UMMA N of the kernel variant serving (Hi, Di, dtype, qb), 0 when no variant exists.
+int indexer_variant_n(int idx_heads, int idx_dim, int fp8, int qb);
+cudaError_t launch_indexer(const IndexerLaunch& launch, cudaStream_t stream);
+
+// ---- sparse flash attention --------------------------------------------------------------------------
+struct SfaParams {
+    const uint16_t* q;         // [T, Hq, D] bf16 bits
+    const uint16_t* kv_cache;  // [num_pages, 64, D] bf16 bits
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const int32_t* cu_q_lens;
+    const int32_t* topk;  // [T, K]
+    uint16_t* out;        // [T, Hq, Dv] bf16 bits
+    float* lse;           // [T, Hq] or null
+    int32_t* err;
+    int32_t batch;
+    int32_t total_q;
+    int32_t num_pages;
+    int32_t max_pages;
+    int32_t top_k;
+    int32_t heads;
+    int32_t kv_dim;
+    int32_t v_dim;
+    float scale_log2;  // softmax_scale * log2(e)
+    int32_t splits;    // position splits per query (filled in by the launcher)
+};
+
+struct SfaLaunch {
+    SfaParams params;
+    int smem_limit;
+    int num_sms;
+};
+
+cudaError_t launch_sfa(const SfaLaunch& launch, cudaStream_t stream);
+
+}  // namespace dsa

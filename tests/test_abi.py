@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads and exports every entry point of include/dsa.h; host-side validation
+answers before any launch.  No GPU needed: nothing here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_dsa_gb300 as dsa
+from sparse_attention_dsa_gb300 import build as dsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    dsa_build.build()
+    return dsa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/dsa.h but not exported"
+    assert set(names) == set(dsa.EXPORTED)
+
+
+def test_abi_version_and_status_strings(L):
+    assert dsa.abi_version() == 1
+    for s in range(6):
+        assert dsa.status_string(s).startswith("DSA_")
+    assert "unknown" in dsa.status_string(99)
+
+
+def _dims(**kw):
+    d = dict(batch=2, total_q=2, max_q_len=1, num_pages=8, page_size=64, max_pages_per_seq=4, idx_heads=64,
+             idx_dim=128, idx_dtype=0, top_k=16, attn_heads=128, kv_dim=576, v_dim=512, softmax_scale=1 / 24)
+    d.update(kw)
+    return dsa.DsaDims(**d)
+
+
+def test_workspace_size(L):
+    assert dsa.workspace_size(_dims()) >= 256
+    assert L.dsa_workspace_size(None) == 0
+
+
+FAKE = 0x10000  # an aligned non-null value; validation rejects the call before it is ever dereferenced
+
+
+def _indexer(d, **ptrs):
+    p = dict(q_idx=FAKE, q_scale=None, w=FAKE, k_cache=FAKE, k_scale=None, page_table=FAKE, seq_lens=FAKE,
+             cu_q_lens=FAKE, topk=FAKE, ws=FAKE)
+    p.update(ptrs)
+    return dsa.lib().dsa_indexer_topk(ctypes.byref(d) if d is not None else None, p["q_idx"], p["q_scale"], p["w"],
+                                      p["k_cache"], p["k_scale"], p["page_table"], p["seq_lens"], p["cu_q_lens"],
+                                      p["topk"], p["ws"], None)
+
+
+def _sfa(d, **ptrs):
+    p = dict(q=FAKE, kv=FAKE, page_table=FAKE, seq_lens=FAKE, cu_q_lens=FAKE, topk=FAKE, out=FAKE, lse=None, ws=FAKE)
+    p.update(ptrs)
+    return dsa.lib().dsa_sparse_attn(ctypes.byref(d), p["q"], p["kv"], p["page_table"], p["seq_lens"],
+                                     p["cu_q_lens"], p["topk"], p["out"], p["lse"], p["ws"], None)
+
+
+def _msg():
+    return dsa.lib().dsa_last_error_message().decode()
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, dsa.DSA_ERR_INVALID_ARG),
+    ("total_q", -1, dsa.DSA_ERR_INVALID_ARG),
+    ("max_q_len", 0, dsa.DSA_ERR_INVALID_ARG),
+    ("num_pages", 0, dsa.DSA_ERR_INVALID_ARG),
+    ("page_size", 32, dsa.DSA_ERR_UNSUPPORTED),
+    ("page_size", -64, dsa.DSA_ERR_INVALID_ARG),
+    ("max_pages_per_seq", 0, dsa.DSA_ERR_INVALID_ARG),
+    ("top_k", 0, dsa.DSA_ERR_INVALID_ARG),
+    ("top_k", 1 << 20, dsa.DSA_ERR_UNSUPPORTED),
+])
+def test_indexer_rejects_bad_dims(L, field, value, status):
+    assert _indexer(_dims(**{field: value})) == status
+    assert field.split("_")[0] in _msg() or "page_size" in _msg()
+
+
+def test_indexer_rejects_null_and_misaligned_pointers(L):
+    assert _indexer(None) == dsa.DSA_ERR_INVALID_ARG
+    assert _indexer(_dims(), q_idx=None) == dsa.DSA_ERR_INVALID_ARG and "q_idx" in _msg()
+    assert _indexer(_dims(), k_cache=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG and "aligned" in _msg()
+    assert _indexer(_dims(), ws=None) == dsa.DSA_ERR_INVALID_ARG and "workspace" in _msg()
+    # FP8 needs both scale arrays
+    assert _indexer(_dims(idx_dtype=1)) == dsa.DSA_ERR_INVALID_ARG and "scale" in _msg()
+    assert _indexer(_dims(idx_dtype=7)) != dsa.DSA_OK
+
+
+def test_sfa_rejects_bad_arguments(L):
+    assert _sfa(_dims(kv_dim=512)) == dsa.DSA_ERR_UNSUPPORTED
+    assert _sfa(_dims(v_dim=600)) == dsa.DSA_ERR_INVALID_ARG
+    assert _sfa(_dims(attn_heads=0)) == dsa.DSA_ERR_INVALID_ARG
+    assert _sfa(_dims(attn_heads=256)) == dsa.DSA_ERR_UNSUPPORTED
+    assert _sfa(_dims(softmax_scale=0.0)) == dsa.DSA_ERR_INVALID_ARG
+    assert _sfa(_dims(), out=None) == dsa.DSA_ERR_INVALID_ARG
+    assert _sfa(_dims(), lse=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_device_error_helpers_validate(L):
+    code = ctypes.c_int32(0)
+    assert L.dsa_get_device_error(None, None, ctypes.byref(code)) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_clear_device_error(None, None) == dsa.DSA_ERR_INVALID_ARG
