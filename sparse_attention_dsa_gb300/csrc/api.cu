@@ -280,6 +280,18 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
     p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
     L.smem_limit = dev.smem_optin;
     L.num_sms = dev.num_sms;
+    {
+        EncodeTiledFn enc = encode_fn();
+        if (!enc) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        const cuuint64_t gdim[2] = {(cuuint64_t)d->kv_dim, (cuuint64_t)d->total_q * d->attn_heads};
+        const cuuint64_t gstride[1] = {(cuuint64_t)d->kv_dim * 2};
+        const cuuint32_t box[2] = {64, 128};
+        const cuuint32_t es[2] = {1, 1};
+        CUresult r = enc(&L.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), gdim, gstride, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "tensor map for q: CUresult %d", (int)r);
+    }
     cudaError_t e = dsa::launch_sfa(L, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
     return DSA_OK;

@@ -71,6 +71,7 @@ struct SfaParams {
 };
 
 struct SfaLaunch {
+    CUtensorMap qmap;  // 2-D view [T*Hq][576] of q, 128-row boxes
     SfaParams params;
     int smem_limit;
     int num_sms;

@@ -107,13 +107,427 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32) sfa_warp_kernel(const SfaPa
     if (p.lse && lane == 0) p.lse[(int64_t)t * p.heads + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
 }
 
+// ======================================================================================================
+// Tensor-core kernel (tcgen05).  One CTA pair per (query token, position split):
+//   * the 128 query heads are the UMMA M dimension; Q[t] (128 x 576 bf16, 144 KiB) stays in smem;
+//   * the selected rows are gathered 32 at a time (cp.async, 16-byte pieces, written straight into the
+//     128B-swizzled operand layout) into a 2-stage ring;
+//   * S = Q K^T (M=128, N=32, K=576) lands in TMEM; softmax warps (one thread per head row) turn it
+//     into P (bf16, smem) with an online max that is only raised when it grows by more than 2^8
+//     (so O rarely needs rescaling);
+//   * O += P V (M=128, N=256, K=32) accumulates in TMEM.  The 512 value dims are split between the
+//     two CTAs of the pair (each owns 256 columns of O), because a full 128 x 512 fp32 O would fill
+//     all of TMEM; both CTAs compute the same S.
+//   * With more than one position split, the partial (O, max, sum) of the splits are merged through
+//     distributed shared memory inside the cluster.
+// ======================================================================================================
+constexpr int kTcThreads = 224;  // warp 0/6: gather (even/odd tiles), 1: MMA, 2-5: softmax
+constexpr int kRows = 32;        // selected rows per tile
+constexpr int kQBytes = 128 * kDim * 2;
+constexpr int kKvStage = kRows * kDim * 2;
+constexpr int kPBytes = 128 * kRows * 2;
+constexpr int kOCols = 256;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kIdescQK = make_idesc(128, kRows, 1, 1, 0, 0);
+constexpr uint32_t kIdescPV = make_idesc(128, kOCols, 1, 1, 0, 1);
+constexpr float kRescaleLog2 = 8.f;  // raise the running max only when it grows by more than this
+
+struct SfaCtrl {
+    uint64_t q_full;
+    uint64_t kv_full[2];
+    uint64_t kv_empty[2];
+    uint64_t s_full[2];
+    uint64_t s_empty[2];
+    uint64_t p_full;
+    uint64_t p_empty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t q_waited;
+    float2 ml[128];
+};
+
+constexpr size_t kTcSmem = 1024 + kQBytes + 2 * kKvStage + kPBytes + sizeof(SfaCtrl);
+
+struct RowRef {
+    const uint16_t* src;
+    bool valid;
+};
+
+// Selected entry e of token t: validity and source row (entries outside [-1, pos] or on a bad page are
+// reported and skipped).
+__device__ __forceinline__ RowRef resolve_entry(const SfaParams& p, int t, int b, int64_t pos, int e, int e_end,
+                                                bool report) {
+    RowRef r{nullptr, false};
+    if (e >= e_end) return r;
+    const int32_t s = __ldg(p.topk + (int64_t)t * p.top_k + e);
+    if (s < 0) return r;
+    if ((int64_t)s > pos) {
+        if (report) raise_error(p.err, DSA_DEVERR_INDEX);
+        return r;
+    }
+    const int32_t pg = __ldg(p.page_table + (int64_t)b * p.max_pages + (s >> 6));
+    if (pg < 0 || pg >= p.num_pages) {
+        if (report) raise_error(p.err, DSA_DEVERR_PAGE);
+        return r;
+    }
+    r.src = p.kv_cache + ((int64_t)pg * 64 + (s & 63)) * kDim;
+    r.valid = true;
+    return r;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q_s = smem;
+    uint8_t* kv_s = q_s + kQBytes;
+    uint8_t* p_s = kv_s + 2 * kKvStage;
+    SfaCtrl* ctl = reinterpret_cast<SfaCtrl*>(p_s + kPBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = p.splits;
+    const int dvh = blockIdx.x & 1;
+    const int ps = (blockIdx.x >> 1) % P;
+    const int t = blockIdx.x / (2 * P);
+    if (t >= p.total_q) return;  // uniform over the cluster
+    int b = 0;
+    {
+        int lo = 0, hi = p.batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.cu_q_lens + mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+    }
+    const int cu0 = __ldg(p.cu_q_lens + b), cu1 = __ldg(p.cu_q_lens + b + 1);
+    const int n_b = cu1 - cu0;
+    const int L = __ldg(p.seq_lens + b);
+    if (t < cu0 || t >= cu1 || n_b > L || L > p.max_pages * 64) {
+        if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
+        return;  // uniform over the cluster (same token)
+    }
+    const int64_t pos = (int64_t)L - n_b + (t - cu0);
+    const int per = ((p.top_k + P - 1) / P + kRows - 1) / kRows * kRows;
+    const int e0 = ps * per;
+    const int e_end = min(p.top_k, e0 + per);
+    const int ntiles = e_end > e0 ? (e_end - e0 + kRows - 1) / kRows : 0;
+
+    if (tid == 0) {
+        mbar_init(&ctl->q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl->kv_full[i], 1);
+            mbar_init(&ctl->kv_empty[i], 1);
+            mbar_init(&ctl->s_full[i], 1);
+            mbar_init(&ctl->s_empty[i], 4);
+        }
+        mbar_init(&ctl->p_full, 4);
+        mbar_init(&ctl->p_empty, 1);
+        mbar_init(&ctl->mma_done, 1);
+        ctl->q_waited = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    float m_used = -INFINITY, l_sum = 0.f;  // softmax threads: running max (log2 units) and sum
+    if (warp == 0 || warp == 6) {
+        // ---------------- gather: warp 0 fills even tiles (stage 0), warp 6 odd tiles (stage 1) ----------------
+        const int parity_tiles = warp == 0 ? 0 : 1;
+        if (warp == 0 && lane == 0) {
+            prefetch_tensormap(&qmap);
+            mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+            for (int a = 0; a < kDim / 64; ++a) tma_load_2d(q_s + a * (128 * 128), &qmap, &ctl->q_full, a * 64, t * p.heads);
+        }
+        uint8_t* stage = kv_s + parity_tiles * kKvStage;
+        for (int i = parity_tiles; i < ntiles; i += 2) {
+            if (!mbar_wait(&ctl->kv_empty[parity_tiles], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err)) break;
+            const RowRef own = resolve_entry(p, t, b, pos, e0 + i * kRows + lane, e_end, dvh == 0);
+            const uint32_t vmask = __ballot_sync(0xFFFFFFFFu, own.valid);
+            const uint64_t own_src = reinterpret_cast<uint64_t>(own.src);
+#pragma unroll 1
+            for (int r0 = 0; r0 < kRows; r0 += 4) {
+                const int r = r0 + (lane >> 3);
+                const int c8 = lane & 7;
+                const uint64_t src = __shfl_sync(0xFFFFFFFFu, own_src, r);
+                const bool valid = (vmask >> r) & 1u;
+                const uint32_t row_base = smem_u32(stage) + r * 128 + ((c8 ^ (r & 7)) << 4);
+#pragma unroll
+                for (int a = 0; a < kDim / 64; ++a) {
+                    const uint32_t dst = row_base + a * (kRows * 128);
+                    if (valid) {
+                        cp_async_16(dst, reinterpret_cast<const uint16_t*>(src) + a * 64 + c8 * 8);
+                    } else {
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                    }
+                }
+            }
+            cp_async_commit();
+            cp_async_wait_group<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->kv_full[parity_tiles]);
+        }
+        cp_async_wait_group<0>();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            bool ok = mbar_wait(&ctl->q_full, 0, p.err);
+            ctl->q_waited = ok ? 1 : 0;
+            const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s), p_base = smem_u32(p_s);
+            auto issue_qk = [&](int j) -> bool {
+                const int st = j & 1;
+                const uint32_t ph = ((uint32_t)j >> 1) & 1u;
+                if (!mbar_wait(&ctl->kv_full[st], ph, p.err)) return false;
+                if (!mbar_wait(&ctl->s_empty[st], ph ^ 1u, p.err)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int a = 0; a < kDim / 64; ++a) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc(q_base + a * (128 * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd =
+                            smem_desc(kv_base + st * kKvStage + a * (kRows * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        umma_f16_ss(tmem + kOCols + st * kRows, ad, bd, kIdescQK, (a | kk) != 0);
+                    }
+                }
+                umma_commit(&ctl->s_full[st]);
+                return true;
+            };
+            if (ok && ntiles > 0) ok = issue_qk(0);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                if (i + 1 < ntiles && !issue_qk(i + 1)) break;
+                if (!mbar_wait(&ctl->p_full, (uint32_t)i & 1u, p.err)) break;
+                tc_fence_after();
+                const int st = i & 1;
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk) {
+                    const uint64_t ad = smem_desc(p_base + kk * 32, 16, 512, kSwizzle64B);
+                    const uint64_t bd = smem_desc(kv_base + st * kKvStage + (dvh * 4) * (kRows * 128) + kk * 2048,
+                                                  kRows * 128, 1024, kSwizzle128B);
+                    umma_f16_ss(tmem, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&ctl->kv_empty[st]);
+                umma_commit(&ctl->p_empty);
+            }
+            umma_commit(&ctl->mma_done);
+            mbar_wait(&ctl->mma_done, 0, p.err);
+        }
+    } else {
+        // ---------------- softmax: one thread per head row ----------------
+        const uint32_t quad = (uint32_t)(warp & 3);
+        const int h = (int)quad * 32 + lane;
+        const uint32_t trow = tmem + ((quad * 32u) << 16);
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i & 1;
+            const RowRef own = resolve_entry(p, t, b, pos, e0 + i * kRows + lane, e_end, false);
+            const uint32_t vmask = __ballot_sync(0xFFFFFFFFu, own.valid);
+            if (!mbar_wait(&ctl->s_full[st], ((uint32_t)i >> 1) & 1u, p.err)) break;
+            tc_fence_after();
+            float sv[32];
+            {
+                float a0[16], a1[16];
+                tmem_ld16(trow + kOCols + st * kRows, a0);
+                tmem_ld16(trow + kOCols + st * kRows + 16, a1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    sv[j] = a0[j];
+                    sv[16 + j] = a1[j];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->s_empty[st]);
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kRows; ++j) {
+                sv[j] = ((vmask >> j) & 1u) ? sv[j] * p.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sv[j]);
+            }
+            const bool raise = mt > m_used + kRescaleLog2;
+            const float m_new = raise ? mt : m_used;
+            // O and the P buffer are free once the previous P.V has completed
+            if (!mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) break;
+            tc_fence_after();
+            const float alpha = (raise && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
+            const bool rescale_warp = __any_sync(0xFFFFFFFFu, alpha != 1.f);
+            if (rescale_warp) {
+#pragma unroll 1
+                for (int c = 0; c < kOCols / 16; ++c) {
+                    float o[16];
+                    tmem_ld16(trow + c * 16, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] *= alpha;
+                    tmem_st16(trow + c * 16, o);
+                }
+                tmem_st_wait();
+            }
+            l_sum *= alpha;
+            m_used = m_new;
+            uint32_t packed[16];
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < kRows; j += 2) {
+                const float e0v = m_used == -INFINITY ? 0.f : exp2f(sv[j] - m_used);
+                const float e1v = m_used == -INFINITY ? 0.f : exp2f(sv[j + 1] - m_used);
+                const uint32_t pk = f2_to_bf2(e0v, e1v);
+                packed[j / 2] = pk;
+                rs += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+            }
+            l_sum += rs;
+            const uint32_t prow = smem_u32(p_s) + h * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t dst = prow + ((c ^ ((h >> 1) & 3)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * c]),
+                             "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->p_full);
+        }
+        if (ntiles > 0) mbar_wait(&ctl->p_empty, ((uint32_t)(ntiles - 1)) & 1u, p.err);
+        tc_fence_after();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0 && lane == 0 && !ctl->q_waited) mbar_wait(&ctl->q_full, 0, p.err);
+
+    // ---------------- epilogue ----------------
+    const bool softmax_thread = warp >= 2 && warp < 6;
+    const int h = softmax_thread ? (warp & 3) * 32 + lane : 0;
+    const uint32_t trow = tmem + (((uint32_t)(warp & 3) * 32u) << 16);
+    if (P == 1) {
+        if (softmax_thread) {
+            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kOCols / 16; ++c) {
+                float o[16];
+                tmem_ld16(trow + c * 16, o);
+                tmem_ld_wait();
+                if (h < p.heads) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) pk[j] = f2_to_bf2(o[2 * j] * inv, o[2 * j + 1] * inv);
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)t * p.heads + h) * kVDim + dvh * kOCols + c * 16);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
+            if (dvh == 0 && h < p.heads && p.lse)
+                p.lse[(int64_t)t * p.heads + h] = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+        }
+    } else {
+        // merge the P position splits of this value half through distributed shared memory
+        if (softmax_thread) ctl->ml[h] = make_float2(m_used, l_sum);
+        cluster_sync();
+        float* obuf = reinterpret_cast<float*>(q_s);  // Q is dead: every MMA has completed
+        float M = -INFINITY, Lsum = 0.f;
+        if (softmax_thread) {
+            float2 ml[8];
+            const uint32_t ml_addr = smem_u32(&ctl->ml[h]);
+            for (int j = 0; j < P; ++j) {
+                const uint32_t a = mapa_shared(ml_addr, (uint32_t)(dvh + 2 * j));
+                float2 v;
+                asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+                ml[j] = v;
+                M = fmaxf(M, v.x);
+            }
+            for (int j = 0; j < P; ++j)
+                if (ml[j].y > 0.f) Lsum += ml[j].y * exp2f(ml[j].x - M);
+            const float f = (l_sum > 0.f && Lsum > 0.f) ? exp2f(m_used - M) / Lsum : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kOCols / 16; ++c) {
+                float o[16];
+                tmem_ld16(trow + c * 16, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int qc = c * 4 + q4;  // 16-byte chunk index 0..63
+                    const uint32_t dst = smem_u32(obuf) + h * 1024 + ((qc ^ (h & 63)) << 4);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(o[4 * q4] * f),
+                                 "f"(o[4 * q4 + 1] * f), "f"(o[4 * q4 + 2] * f), "f"(o[4 * q4 + 3] * f)
+                                 : "memory");
+                }
+            }
+            const int slice = 128 / P;
+            if (dvh == 0 && h / slice == ps && h < p.heads && p.lse)
+                p.lse[(int64_t)t * p.heads + h] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        }
+        cluster_sync();
+        if (softmax_thread) {
+            const int slice = 128 / P;
+            const int h0 = ps * slice;
+            const int stid = tid - 64;  // 0..127
+            for (int idx = stid; idx < slice * 64; idx += 128) {
+                const int hh = h0 + idx / 64;
+                const int qc = idx % 64;
+                if (hh >= p.heads) continue;
+                const uint32_t local = smem_u32(obuf) + hh * 1024 + ((qc ^ (hh & 63)) << 4);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < P; ++j) {
+                    const float4 v = ld_dsmem_f4(mapa_shared(local, (uint32_t)(dvh + 2 * j)));
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                uint2 pk = make_uint2(f2_to_bf2(acc.x, acc.y), f2_to_bf2(acc.z, acc.w));
+                *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + hh) * kVDim + dvh * kOCols + qc * 4) = pk;
+            }
+        }
+        cluster_sync();  // peers may still be reading this CTA's buffers
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
 }  // namespace
 
+bool sfa_use_tensor_cores = true;
+
 cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
-    const SfaParams& p = L.params;
-    dim3 grid((unsigned)p.total_q, (unsigned)((p.heads + kHeadsPerCta - 1) / kHeadsPerCta));
-    sfa_warp_kernel<<<grid, kHeadsPerCta * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    const SfaParams& p0 = L.params;
+    if (!sfa_use_tensor_cores) {
+        dim3 grid((unsigned)p0.total_q, (unsigned)((p0.heads + kHeadsPerCta - 1) / kHeadsPerCta));
+        sfa_warp_kernel<<<grid, kHeadsPerCta * 32, 0, stream>>>(p0);
+        return cudaGetLastError();
+    }
+    SfaParams p = p0;
+    int P = 1;
+    const int max_splits = (p.top_k + kRows - 1) / kRows;
+    while (P < 8 && P * 2 <= max_splits && (int64_t)p.total_q * 2 * (P * 2) <= L.num_sms) P *= 2;
+    p.splits = P;
+    if (kTcSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)(P == 1 ? 1 : 2 * P);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(p.total_q * 2 * P));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sfa_tc_kernel, L.qmap, p);
 }
 
 }  // namespace dsa
