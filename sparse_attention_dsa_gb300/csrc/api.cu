@@ -246,6 +246,8 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
         return fail(DSA_ERR_UNSUPPORTED, "sparse attention supports kv_dim 576 / v_dim 512 (got %d / %d)", d->kv_dim,
                     d->v_dim);
     if (d->attn_heads > 128) return fail(DSA_ERR_UNSUPPORTED, "attn_heads must be <= 128 (got %d)", d->attn_heads);
+    if ((int64_t)d->num_pages * 64 > (int64_t)INT32_MAX)
+        return fail(DSA_ERR_UNSUPPORTED, "num_pages * 64 must fit in int32 (got %d pages)", d->num_pages);
     if (!(d->softmax_scale > 0.f) || d->softmax_scale > 1e30f)
         return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be a positive finite number");
     if ((st = check_ptr(q, "q")) || (st = check_ptr(kv_cache, "kv_cache")) ||

@@ -36,6 +36,7 @@ constexpr int kThreads = 256;
 constexpr int kTileM = 128;  // positions per tile (two pages)
 constexpr int kPage = 64;
 constexpr int kMaxCluster = 16;
+constexpr int kPrefetchTiles = 4;  // tiles prefetched into L2 beyond the smem ring
 
 template <int HI, int DI, int QB, bool FP8>
 struct IdxCfg {
@@ -57,7 +58,6 @@ struct IdxCfg {
 
 struct SelectSmem {
     uint32_t hist[2][256];
-    uint32_t allh[kMaxCluster][256];
     uint32_t totals[256];
     uint32_t gt[kMaxCluster];
     uint32_t ecnt[kMaxCluster];
@@ -88,10 +88,12 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // Cluster-wide Top-K of one query.  keys: this CTA's n local keys (position range_start + i);
-// visible = p + 1 positions exist in total.  All CTAs of the cluster call this with identical
-// (K, visible), so the cluster barriers inside match up.
-__device__ void cluster_select(const uint32_t* keys, int n, int K, int64_t visible, int32_t* out_row,
-                               int range_start, uint32_t rank, uint32_t C, SelectSmem& S) {
+// hist0: this CTA's histogram of the keys' top byte, built while scoring; allh: C x 256 scratch for the
+// gathered per-CTA histograms.  visible = p + 1 positions exist in total.  All CTAs of the cluster call
+// this with identical (K, visible), so the cluster barriers inside match up.
+__device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, int n, int K,
+                               int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
+                               SelectSmem& S) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (visible <= K) {  // every visible position is kept: 0..p in order, then -1
         const int per = (K + (int)C - 1) / (int)C;
@@ -105,23 +107,25 @@ __device__ void cluster_select(const uint32_t* keys, int n, int K, int64_t visib
         const int shift = 24 - 8 * pass;
         const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
         const int buf = pass & 1;
-        S.hist[buf][tid] = 0;
-        __syncthreads();
-        for (int i = tid; i < n; i += kThreads) {
-            const uint32_t key = keys[i];
-            if (((key ^ prefix) & hmask) == 0) {
-                const uint32_t bin = (key >> shift) & 255u;
-                const uint32_t peers = __match_any_sync(__activemask(), bin);
-                if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[buf][bin], (uint32_t)__popc(peers));
+        if (pass > 0) {  // the top-byte histogram (pass 0) was built while scoring
+            S.hist[buf][tid] = 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t key = keys[i];
+                if (((key ^ prefix) & hmask) == 0) {
+                    const uint32_t bin = (key >> shift) & 255u;
+                    const uint32_t peers = __match_any_sync(__activemask(), bin);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[buf][bin], (uint32_t)__popc(peers));
+                }
             }
         }
         cluster_sync();
         {
             uint32_t tot = 0;
-            const uint32_t local = smem_u32(&S.hist[buf][tid]);
+            const uint32_t local = pass == 0 ? smem_u32(hist0 + tid) : smem_u32(&S.hist[buf][tid]);
             for (uint32_t r = 0; r < C; ++r) {
                 const uint32_t v = ld_dsmem_u32(mapa_shared(local, r));
-                S.allh[r][tid] = v;
+                allh[r * 256 + tid] = v;
                 tot += v;
             }
             S.totals[tid] = tot;
@@ -154,12 +158,12 @@ __device__ void cluster_select(const uint32_t* keys, int n, int K, int64_t visib
         const uint32_t bstar = S.bstar;
         for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
             uint32_t s = 0;
-            for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? S.allh[r][i] : 0u;
+            for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? allh[r * 256 + i] : 0u;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
             if (lane == 0) S.gt[r] += s;
         }
-        if (pass == 3 && tid < (int)C) S.ecnt[tid] = S.allh[tid][bstar];
+        if (pass == 3 && tid < (int)C) S.ecnt[tid] = allh[tid * 256 + bstar];
         remaining = S.remaining;
         prefix |= bstar << shift;
         __syncthreads();
@@ -226,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* keys = reinterpret_cast<uint32_t*>(q_tile + Cfg::kQBytes);  // QB * chunk
     float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
     int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64
-    SelectSmem* sel = reinterpret_cast<SelectSmem*>(pages_s + p.chunk / kPage);
+    uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + p.chunk / kPage);  // QB x 256
+    uint32_t* allh = hist0 + QB * 256;                                      // C x 256
+    SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + cluster_nctarank() * 256);
     CtrlSmem* ctl = reinterpret_cast<CtrlSmem*>((reinterpret_cast<uintptr_t>(sel + 1) + 15) & ~uintptr_t(15));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -273,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pages_s[i] = pg;
     }
+    for (int i = tid; i < QB * 256; i += kThreads) hist0[i] = 0;
     for (int c = tid; c < Cfg::kN; c += kThreads) {
         float wv = 0.f;
         if (c < nq * HI) {
@@ -315,10 +322,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int a = 0; a < Cfg::kAtoms; ++a)
                     tma_load_2d(q_tile + a * Cfg::kN * 128, &qmap, &ctl->qbar, a * (128 / Cfg::kElem), t0 * HI);
+                // L2 prefetch keeps kPrefetchTiles more tiles in flight than the smem ring holds
+                auto prefetch_tile = [&](int j) {
+                    if (j >= ntiles) return;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int32_t pg = pages_s[2 * j + h2];
+                        if (pg < 0) continue;
+#pragma unroll
+                        for (int a = 0; a < Cfg::kAtoms; ++a) tma_prefetch_3d(&kmap, a * (128 / Cfg::kElem), 0, pg);
+                    }
+                };
+                for (int j = S; j < S + kPrefetchTiles; ++j) prefetch_tile(j);
                 int issued = 0;
                 for (int i = 0; i < ntiles; ++i) {
                     const int s = i % S;
                     const uint32_t ph = (uint32_t)(i / S) & 1u;
+                    prefetch_tile(i + S + kPrefetchTiles);
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1u, p.err)) break;
                     const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
                     const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * (kPage * Cfg::kRowBytes);
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t pg = pages_s[2 * i + (row >> 6)];
                 float ksc = 1.f;
                 if (FP8 && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
-                if (!mbar_wait(&ctl->tfull[ab], aph, p.err)) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err))) break;
                 tc_fence_after();
                 float acc[QB];
 #pragma unroll
@@ -421,6 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t key = 0;
                     if (q < nq && pg >= 0 && (int64_t)pos <= pq[q]) key = score_key(FP8 ? acc[q] * ksc : acc[q]);
                     keys[q * p.chunk + local] = key;
+                    // top-byte histogram for the first radix pass (warp-aggregated)
+                    const uint32_t bin = key >> 24;
+                    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&hist0[q * 256 + bin], (uint32_t)__popc(peers));
                 }
             }
         }
@@ -440,17 +464,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- cluster-wide Top-K per query -------------------------------------------------------------------
     for (int q = 0; q < nq; ++q) {
         const int64_t visible = (int64_t)L - n_b + j0 + q + 1;
-        cluster_select(keys + (size_t)q * p.chunk, n_keys, p.top_k, visible, p.topk + (int64_t)(t0 + q) * p.top_k,
-                       range_start, rank, C, *sel);
+        cluster_select(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, n_keys, p.top_k, visible,
+                       p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel);
     }
     cluster_sync();  // peers may still read this CTA's histograms
 }
 
 template <int HI, int DI, int QB, bool FP8>
-size_t indexer_smem_bytes(int stages, int chunk) {
+size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
     using Cfg = IdxCfg<HI, DI, QB, FP8>;
     return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
-           (size_t)(chunk / kPage) * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) + 64;
+           (size_t)(chunk / kPage) * 4 + (size_t)(QB + cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
+           64;
 }
 
 template <int HI, int DI, int QB, bool FP8>
@@ -460,8 +485,8 @@ cudaError_t launch_variant(const IndexerLaunch& L, cudaStream_t stream) {
     const int chunk = L.params.chunk;
     // choose the number of pipeline stages from the shared-memory budget
     int stages = kMaxStages;
-    while (stages > 2 && indexer_smem_bytes<HI, DI, QB, FP8>(stages, chunk) > (size_t)L.smem_limit) --stages;
-    const size_t smem = indexer_smem_bytes<HI, DI, QB, FP8>(stages, chunk);
+    while (stages > 2 && indexer_smem_bytes<HI, DI, QB, FP8>(stages, chunk, L.cluster) > (size_t)L.smem_limit) --stages;
+    const size_t smem = indexer_smem_bytes<HI, DI, QB, FP8>(stages, chunk, L.cluster);
     if (smem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
     IndexerParams prm = L.params;
     prm.stages = stages;

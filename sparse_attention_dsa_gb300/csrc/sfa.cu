@@ -4,11 +4,25 @@
 // out[t,h,:] = softmax(z) . kv[:, :Dv], lse = logsumexp(z) ("Optimizing Inference for Hybrid Attention
 // Architectures: From Operator Fusion to Sequence Sharding", section "Breaking Down the Computational
 // Path of Hybrid Attention", step 2; "Day0 Inference Support and Performance Optimization for New LLM
-// Architectures", section 3.2: only the selected positions' KV rows are read).
+// Architectures", section 3.2: only the selected positions' KV rows are read; "Optimizing Inference for
+// Hybrid Attention LLMs: Practices for Fast Adaptation", section 3.2: gather of the next rows overlaps
+// the computation on the current ones).
 //
-// This translation unit holds the warp-per-head kernel: one warp per (token, head); every warp of a
-// CTA walks the same selected rows, so each gathered row is read from L2 once per CTA and served to
-// the other warps from L1.  Online softmax in fp32 (base-2 exponent), fp32 accumulation.
+// One CTA pair per (query token, position split):
+//   * the 128 query heads are the UMMA M dimension; Q[t] (128 x 576 bf16, 144 KiB) stays in smem;
+//   * at start every thread helps translate the split's selected positions (Top-K entry -> page table
+//     -> physical row) into a row list in smem, so no global lookup sits on the per-tile path;
+//   * two gather warps copy the selected rows 32 at a time (cp.async, 16-byte pieces written straight
+//     into the 128B-swizzled operand layout) into a 2-stage ring, and prefetch rows a few tiles ahead
+//     into L2 (cp.async.bulk.prefetch) to keep more bytes in flight than the ring holds;
+//   * S = Q K^T (M=128, N=32, K=576) lands in TMEM; softmax warps (one thread per head row) turn it into
+//     P (bf16) stored back into TMEM, with an online max that is only raised when it grows by more than
+//     2^8 (so O rarely needs rescaling);
+//   * O += P V (M=128, N=256, K=32; A = P from TMEM, B = the same smem rows read as MN-major V)
+//     accumulates in TMEM.  The 512 value dims are split between the two CTAs of the pair (each owns 256
+//     columns of O) because a full 128 x 512 fp32 O would fill all of TMEM; both CTAs compute the same S.
+//   * With more than one position split, the partial (O, max, sum) of the splits are merged through
+//     distributed shared memory inside the cluster.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,116 +32,18 @@
 namespace dsa {
 namespace {
 
-constexpr int kHeadsPerCta = 8;
 constexpr int kDim = 576;  // latent + rope
 constexpr int kVDim = 512;
-constexpr int kPairs = kDim / 64;   // bf16 pairs per lane: lane owns dims 2*lane + 64*j (+1)
-constexpr int kVPairs = kVDim / 64;
-
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-}
-__device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
-    // round to nearest even (finite inputs)
-    uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
-    ua += 0x7FFFu + ((ua >> 16) & 1u);
-    ub += 0x7FFFu + ((ub >> 16) & 1u);
-    return (ua >> 16) | (ub & 0xFFFF0000u);
-}
-
-__global__ void __launch_bounds__(kHeadsPerCta * 32) sfa_warp_kernel(const SfaParams p) {
-    const int t = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y * kHeadsPerCta + warp;
-    if (t >= p.total_q || h >= p.heads) return;
-    // sequence of this token
-    int b = 0;
-    {
-        int lo = 0, hi = p.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.cu_q_lens[mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-    }
-    const int n_b = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
-    const int L = p.seq_lens[b];
-    if (t < p.cu_q_lens[b] || t >= p.cu_q_lens[b + 1] || n_b > L || L > p.max_pages * 64) {
-        if (lane == 0) raise_error(p.err, DSA_DEVERR_SEQ);
-        return;
-    }
-    const int64_t pos = (int64_t)L - n_b + (t - p.cu_q_lens[b]);
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)t * p.heads + h) * kDim);
-    float2 q[kPairs];
-#pragma unroll
-    for (int j = 0; j < kPairs; ++j) q[j] = bf2_to_f2(__ldg(qrow + lane + 32 * j));
-    float m = -INFINITY, l = 0.f;
-    float2 o[kVPairs];
-#pragma unroll
-    for (int j = 0; j < kVPairs; ++j) o[j] = make_float2(0.f, 0.f);
-    const int32_t* sel = p.topk + (int64_t)t * p.top_k;
-    const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
-    for (int k = 0; k < p.top_k; ++k) {
-        const int32_t s = __ldg(sel + k);
-        if (s < 0) continue;
-        if ((int64_t)s > pos) {
-            if (lane == 0 && h == 0) raise_error(p.err, DSA_DEVERR_INDEX);
-            continue;
-        }
-        const int32_t pg = __ldg(pt_row + (s >> 6));
-        if (pg < 0 || pg >= p.num_pages) {
-            if (lane == 0 && h == 0) raise_error(p.err, DSA_DEVERR_PAGE);
-            continue;
-        }
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(p.kv_cache + ((int64_t)pg * 64 + (s & 63)) * kDim);
-        float2 kv[kPairs];
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j) kv[j] = bf2_to_f2(__ldg(row + lane + 32 * j));
-        float dot = 0.f;
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j) dot = fmaf(q[j].x, kv[j].x, fmaf(q[j].y, kv[j].y, dot));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-        const float z = dot * p.scale_log2;  // base-2 logit
-        const float m_new = fmaxf(m, z);
-        const float corr = exp2f(m - m_new);
-        const float e = exp2f(z - m_new);
-        l = l * corr + e;
-#pragma unroll
-        for (int j = 0; j < kVPairs; ++j) {
-            o[j].x = fmaf(o[j].x, corr, e * kv[j].x);
-            o[j].y = fmaf(o[j].y, corr, e * kv[j].y);
-        }
-        m = m_new;
-    }
-    uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + ((int64_t)t * p.heads + h) * kVDim);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-    for (int j = 0; j < kVPairs; ++j) orow[lane + 32 * j] = f2_to_bf2(o[j].x * inv, o[j].y * inv);
-    if (p.lse && lane == 0) p.lse[(int64_t)t * p.heads + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-}
-
-// ======================================================================================================
-// Tensor-core kernel (tcgen05).  One CTA pair per (query token, position split):
-//   * the 128 query heads are the UMMA M dimension; Q[t] (128 x 576 bf16, 144 KiB) stays in smem;
-//   * the selected rows are gathered 32 at a time (cp.async, 16-byte pieces, written straight into the
-//     128B-swizzled operand layout) into a 2-stage ring;
-//   * S = Q K^T (M=128, N=32, K=576) lands in TMEM; softmax warps (one thread per head row) turn it
-//     into P (bf16, smem) with an online max that is only raised when it grows by more than 2^8
-//     (so O rarely needs rescaling);
-//   * O += P V (M=128, N=256, K=32) accumulates in TMEM.  The 512 value dims are split between the
-//     two CTAs of the pair (each owns 256 columns of O), because a full 128 x 512 fp32 O would fill
-//     all of TMEM; both CTAs compute the same S.
-//   * With more than one position split, the partial (O, max, sum) of the splits are merged through
-//     distributed shared memory inside the cluster.
-// ======================================================================================================
-constexpr int kTcThreads = 224;  // warp 0/6: gather (even/odd tiles), 1: MMA, 2-5: softmax
-constexpr int kRows = 32;        // selected rows per tile
+constexpr int kThreadsSfa = 224;  // warp 0/6: gather (even/odd tiles), 1: MMA, 2-5: softmax
+constexpr int kRows = 32;         // selected rows per tile
 constexpr int kQBytes = 128 * kDim * 2;
 constexpr int kKvStage = kRows * kDim * 2;
-constexpr int kPBytes = 128 * kRows * 2;
+constexpr int kMaxEntries = 2048;  // selected entries per CTA (per position split)
 constexpr int kOCols = 256;
+constexpr int kSCol = 256;  // two S buffers of 32 columns
+constexpr int kPCol = 320;  // P: 32 bf16 per row = 16 columns
 constexpr int kTmemCols = 512;
+constexpr int kPrefetchTiles = 4;  // L2 prefetch distance, in tiles of the same gather warp
 constexpr uint32_t kIdescQK = make_idesc(128, kRows, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = make_idesc(128, kOCols, 1, 1, 0, 1);
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only when it grows by more than this
@@ -146,43 +62,47 @@ struct SfaCtrl {
     float2 ml[128];
 };
 
-constexpr size_t kTcSmem = 1024 + kQBytes + 2 * kKvStage + kPBytes + sizeof(SfaCtrl);
+constexpr size_t kSfaSmem = 1024 + kQBytes + 2 * kKvStage + kMaxEntries * 4 + sizeof(SfaCtrl);
 
-struct RowRef {
-    const uint16_t* src;
-    bool valid;
-};
-
-// Selected entry e of token t: validity and source row (entries outside [-1, pos] or on a bad page are
-// reported and skipped).
-__device__ __forceinline__ RowRef resolve_entry(const SfaParams& p, int t, int b, int64_t pos, int e, int e_end,
-                                                bool report) {
-    RowRef r{nullptr, false};
-    if (e >= e_end) return r;
-    const int32_t s = __ldg(p.topk + (int64_t)t * p.top_k + e);
-    if (s < 0) return r;
-    if ((int64_t)s > pos) {
-        if (report) raise_error(p.err, DSA_DEVERR_INDEX);
-        return r;
-    }
-    const int32_t pg = __ldg(p.page_table + (int64_t)b * p.max_pages + (s >> 6));
-    if (pg < 0 || pg >= p.num_pages) {
-        if (report) raise_error(p.err, DSA_DEVERR_PAGE);
-        return r;
-    }
-    r.src = p.kv_cache + ((int64_t)pg * 64 + (s & 63)) * kDim;
-    r.valid = true;
-    return r;
+__device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
+    // round to nearest even (finite inputs); a in the low half
+    uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    ua += 0x7FFFu + ((ua >> 16) & 1u);
+    ub += 0x7FFFu + ((ub >> 16) & 1u);
+    return (ua >> 16) | (ub & 0xFFFF0000u);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-    sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreadsSfa, 1)
+    sfa_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q_s = smem;
     uint8_t* kv_s = q_s + kQBytes;
-    uint8_t* p_s = kv_s + 2 * kKvStage;
-    SfaCtrl* ctl = reinterpret_cast<SfaCtrl*>(p_s + kPBytes);
+    int32_t* rows_s = reinterpret_cast<int32_t*>(kv_s + 2 * kKvStage);  // physical row per entry, -1 = skip
+    SfaCtrl* ctl = reinterpret_cast<SfaCtrl*>(rows_s + kMaxEntries);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = p.splits;
@@ -209,9 +129,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t pos = (int64_t)L - n_b + (t - cu0);
     const int per = ((p.top_k + P - 1) / P + kRows - 1) / kRows * kRows;
     const int e0 = ps * per;
-    const int e_end = min(p.top_k, e0 + per);
-    const int ntiles = e_end > e0 ? (e_end - e0 + kRows - 1) / kRows : 0;
+    const int n_ent = max(0, min(p.top_k, e0 + per) - e0);
+    const int ntiles = (n_ent + kRows - 1) / kRows;
 
+    // ---- translate this split's entries into physical rows (all threads, independent loads) ----
+    {
+        const int32_t* sel = p.topk + (int64_t)t * p.top_k + e0;
+        const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
+        for (int e = tid; e < ntiles * kRows; e += kThreadsSfa) {
+            int32_t row = -1;
+            if (e < n_ent) {
+                const int32_t s = __ldg(sel + e);
+                if (s >= 0) {
+                    if ((int64_t)s > pos) {
+                        if (dvh == 0) raise_error(p.err, DSA_DEVERR_INDEX);
+                    } else {
+                        const int32_t pg = __ldg(pt_row + (s >> 6));
+                        if (pg < 0 || pg >= p.num_pages) {
+                            if (dvh == 0) raise_error(p.err, DSA_DEVERR_PAGE);
+                        } else {
+                            row = pg * 64 + (s & 63);
+                        }
+                    }
+                }
+            }
+            rows_s[e] = row;
+        }
+    }
     if (tid == 0) {
         mbar_init(&ctl->q_full, 1);
         for (int i = 0; i < 2; ++i) {
@@ -238,40 +182,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_used = -INFINITY, l_sum = 0.f;  // softmax threads: running max (log2 units) and sum
     if (warp == 0 || warp == 6) {
         // ---------------- gather: warp 0 fills even tiles (stage 0), warp 6 odd tiles (stage 1) ----------------
-        const int parity_tiles = warp == 0 ? 0 : 1;
+        const int par = warp == 0 ? 0 : 1;
         if (warp == 0 && lane == 0) {
             prefetch_tensormap(&qmap);
             mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
             for (int a = 0; a < kDim / 64; ++a) tma_load_2d(q_s + a * (128 * 128), &qmap, &ctl->q_full, a * 64, t * p.heads);
         }
-        uint8_t* stage = kv_s + parity_tiles * kKvStage;
-        for (int i = parity_tiles; i < ntiles; i += 2) {
-            if (!mbar_wait(&ctl->kv_empty[parity_tiles], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err)) break;
-            const RowRef own = resolve_entry(p, t, b, pos, e0 + i * kRows + lane, e_end, dvh == 0);
-            const uint32_t vmask = __ballot_sync(0xFFFFFFFFu, own.valid);
-            const uint64_t own_src = reinterpret_cast<uint64_t>(own.src);
+        // warm L2 with this warp's first tiles
+        for (int i = par; i < ntiles && i < par + 2 * kPrefetchTiles; i += 2) {
+            const int32_t row = rows_s[i * kRows + lane];
+            if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
+        }
+        uint8_t* stage = kv_s + par * kKvStage;
+        for (int i = par; i < ntiles; i += 2) {
+            const int ahead = i + 2 * kPrefetchTiles;
+            if (ahead < ntiles) {
+                const int32_t row = rows_s[ahead * kRows + lane];
+                if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
+            }
+            if (!mbar_wait(&ctl->kv_empty[par], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err)) break;
 #pragma unroll 1
             for (int r0 = 0; r0 < kRows; r0 += 4) {
                 const int r = r0 + (lane >> 3);
                 const int c8 = lane & 7;
-                const uint64_t src = __shfl_sync(0xFFFFFFFFu, own_src, r);
-                const bool valid = (vmask >> r) & 1u;
+                const int32_t row = rows_s[i * kRows + r];
+                const uint16_t* src = p.kv_cache + (int64_t)row * kDim + c8 * 8;
                 const uint32_t row_base = smem_u32(stage) + r * 128 + ((c8 ^ (r & 7)) << 4);
 #pragma unroll
                 for (int a = 0; a < kDim / 64; ++a) {
                     const uint32_t dst = row_base + a * (kRows * 128);
-                    if (valid) {
-                        cp_async_16(dst, reinterpret_cast<const uint16_t*>(src) + a * 64 + c8 * 8);
-                    } else {
+                    if (row >= 0)
+                        cp_async_16(dst, src + a * 64);
+                    else
                         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
-                    }
                 }
             }
             cp_async_commit();
             cp_async_wait_group<0>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->kv_full[parity_tiles]);
+            if (lane == 0) mbar_arrive(&ctl->kv_full[par]);
         }
         cp_async_wait_group<0>();
     } else if (warp == 1) {
@@ -279,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             bool ok = mbar_wait(&ctl->q_full, 0, p.err);
             ctl->q_waited = ok ? 1 : 0;
-            const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s), p_base = smem_u32(p_s);
+            const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s);
             auto issue_qk = [&](int j) -> bool {
                 const int st = j & 1;
                 const uint32_t ph = ((uint32_t)j >> 1) & 1u;
@@ -293,7 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t ad = smem_desc(q_base + a * (128 * 128) + kk * 32, 16, 1024, kSwizzle128B);
                         const uint64_t bd =
                             smem_desc(kv_base + st * kKvStage + a * (kRows * 128) + kk * 32, 16, 1024, kSwizzle128B);
-                        umma_f16_ss(tmem + kOCols + st * kRows, ad, bd, kIdescQK, (a | kk) != 0);
+                        umma_f16_ss(tmem + kSCol + st * kRows, ad, bd, kIdescQK, (a | kk) != 0);
                     }
                 }
                 umma_commit(&ctl->s_full[st]);
@@ -307,10 +257,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int st = i & 1;
 #pragma unroll
                 for (int kk = 0; kk < kRows / 16; ++kk) {
-                    const uint64_t ad = smem_desc(p_base + kk * 32, 16, 512, kSwizzle64B);
+                    // V rows of this stage as an MN-major operand: 64-dim atoms 4096 B apart, 8-row groups 1024 B
                     const uint64_t bd = smem_desc(kv_base + st * kKvStage + (dvh * 4) * (kRows * 128) + kk * 2048,
                                                   kRows * 128, 1024, kSwizzle128B);
-                    umma_f16_ss(tmem, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tmem, tmem + kPCol + kk * 8, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&ctl->kv_empty[st]);
                 umma_commit(&ctl->p_empty);
@@ -321,19 +271,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
         // ---------------- softmax: one thread per head row ----------------
         const uint32_t quad = (uint32_t)(warp & 3);
-        const int h = (int)quad * 32 + lane;
         const uint32_t trow = tmem + ((quad * 32u) << 16);
         for (int i = 0; i < ntiles; ++i) {
             const int st = i & 1;
-            const RowRef own = resolve_entry(p, t, b, pos, e0 + i * kRows + lane, e_end, false);
-            const uint32_t vmask = __ballot_sync(0xFFFFFFFFu, own.valid);
+            const uint32_t vmask = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
             if (!mbar_wait(&ctl->s_full[st], ((uint32_t)i >> 1) & 1u, p.err)) break;
             tc_fence_after();
             float sv[32];
             {
                 float a0[16], a1[16];
-                tmem_ld16(trow + kOCols + st * kRows, a0);
-                tmem_ld16(trow + kOCols + st * kRows + 16, a1);
+                tmem_ld16(trow + kSCol + st * kRows, a0);
+                tmem_ld16(trow + kSCol + st * kRows + 16, a1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -352,12 +300,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             const bool raise = mt > m_used + kRescaleLog2;
             const float m_new = raise ? mt : m_used;
-            // O and the P buffer are free once the previous P.V has completed
+            // O and the P columns are free once the previous P.V has completed
             if (!mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) break;
             tc_fence_after();
             const float alpha = (raise && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
-            const bool rescale_warp = __any_sync(0xFFFFFFFFu, alpha != 1.f);
-            if (rescale_warp) {
+            if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll 1
                 for (int c = 0; c < kOCols / 16; ++c) {
                     float o[16];
@@ -367,7 +314,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int j = 0; j < 16; ++j) o[j] *= alpha;
                     tmem_st16(trow + c * 16, o);
                 }
-                tmem_st_wait();
             }
             l_sum *= alpha;
             m_used = m_new;
@@ -375,22 +321,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float rs = 0.f;
 #pragma unroll
             for (int j = 0; j < kRows; j += 2) {
-                const float e0v = m_used == -INFINITY ? 0.f : exp2f(sv[j] - m_used);
-                const float e1v = m_used == -INFINITY ? 0.f : exp2f(sv[j + 1] - m_used);
-                const uint32_t pk = f2_to_bf2(e0v, e1v);
+                const float x0 = m_used == -INFINITY ? 0.f : exp2f(sv[j] - m_used);
+                const float x1 = m_used == -INFINITY ? 0.f : exp2f(sv[j + 1] - m_used);
+                const uint32_t pk = f2_to_bf2(x0, x1);
                 packed[j / 2] = pk;
                 rs += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
             }
             l_sum += rs;
-            const uint32_t prow = smem_u32(p_s) + h * 64;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t dst = prow + ((c ^ ((h >> 1) & 3)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[4 * c]),
-                             "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
-                             : "memory");
-            }
-            fence_proxy_async_smem();
+            tmem_st16_u32(trow + kPCol, packed);
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->p_full);
@@ -419,7 +358,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint32_t pk[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) pk[j] = f2_to_bf2(o[2 * j] * inv, o[2 * j + 1] * inv);
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)t * p.heads + h) * kVDim + dvh * kOCols + c * 16);
+                    uint4* dst =
+                        reinterpret_cast<uint4*>(p.out + ((int64_t)t * p.heads + h) * kVDim + dvh * kOCols + c * 16);
                     dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
@@ -432,19 +372,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (softmax_thread) ctl->ml[h] = make_float2(m_used, l_sum);
         cluster_sync();
         float* obuf = reinterpret_cast<float*>(q_s);  // Q is dead: every MMA has completed
-        float M = -INFINITY, Lsum = 0.f;
         if (softmax_thread) {
+            float M = -INFINITY, Lsum = 0.f;
             float2 ml[8];
             const uint32_t ml_addr = smem_u32(&ctl->ml[h]);
-            for (int j = 0; j < P; ++j) {
-                const uint32_t a = mapa_shared(ml_addr, (uint32_t)(dvh + 2 * j));
-                float2 v;
-                asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-                ml[j] = v;
-                M = fmaxf(M, v.x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j < P) {
+                    const uint32_t a = mapa_shared(ml_addr, (uint32_t)(dvh + 2 * j));
+                    float2 v;
+                    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+                    ml[j] = v;
+                    M = fmaxf(M, v.x);
+                }
             }
-            for (int j = 0; j < P; ++j)
-                if (ml[j].y > 0.f) Lsum += ml[j].y * exp2f(ml[j].x - M);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < P && ml[j].y > 0.f) Lsum += ml[j].y * exp2f(ml[j].x - M);
             const float f = (l_sum > 0.f && Lsum > 0.f) ? exp2f(m_used - M) / Lsum : 0.f;
 #pragma unroll 1
             for (int c = 0; c < kOCols / 16; ++c) {
@@ -482,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     acc.z += v.z;
                     acc.w += v.w;
                 }
-                uint2 pk = make_uint2(f2_to_bf2(acc.x, acc.y), f2_to_bf2(acc.z, acc.w));
+                const uint2 pk = make_uint2(f2_to_bf2(acc.x, acc.y), f2_to_bf2(acc.z, acc.w));
                 *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + hh) * kVDim + dvh * kOCols + qc * 4) = pk;
             }
         }
@@ -496,24 +440,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
-bool sfa_use_tensor_cores = true;
-
 cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
-    const SfaParams& p0 = L.params;
-    if (!sfa_use_tensor_cores) {
-        dim3 grid((unsigned)p0.total_q, (unsigned)((p0.heads + kHeadsPerCta - 1) / kHeadsPerCta));
-        sfa_warp_kernel<<<grid, kHeadsPerCta * 32, 0, stream>>>(p0);
-        return cudaGetLastError();
-    }
-    SfaParams p = p0;
+    SfaParams p = L.params;
+    // position splits: enough CTAs to cover the SMs, and at most kMaxEntries entries per split
     int P = 1;
+    while (P < 8 && (p.top_k + P - 1) / P > kMaxEntries) P *= 2;
     const int max_splits = (p.top_k + kRows - 1) / kRows;
     while (P < 8 && P * 2 <= max_splits && (int64_t)p.total_q * 2 * (P * 2) <= L.num_sms) P *= 2;
+    if ((p.top_k + P - 1) / P > kMaxEntries) return cudaErrorInvalidValue;
     p.splits = P;
-    if (kTcSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    if (kSfaSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSfaSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -522,12 +461,12 @@ cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(p.total_q * 2 * P));
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.blockDim = dim3(kThreadsSfa);
+    cfg.dynamicSmemBytes = kSfaSmem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sfa_tc_kernel, L.qmap, p);
+    return cudaLaunchKernelEx(&cfg, sfa_kernel, L.qmap, p);
 }
 
 }  // namespace dsa
