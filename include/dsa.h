@@ -152,6 +152,28 @@ dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const f
                               int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream);
 
 /*
+ * dsa_indexer_topk without a workspace argument.  The articles have no counterpart to this call; it
+ * exists for callers that cannot allocate device memory when they run the indexer: code living inside
+ * another runtime that owns all device memory (a pooled allocator or a server that forbids raw
+ * cudaMalloc), decode loops that must not allocate after start-up, and plug-in hosts that offer no
+ * allocator.  The kernels are those of dsa_indexer_topk and so are the arguments, except:
+ *   - the scratch (the device error word) lives in a static device array of 4096 bytes inside the
+ *     library; every GPU that loads the library holds it until the process exits.  Dims whose
+ *     dsa_workspace_size() exceeds 4096 bytes are rejected with DSA_ERR_UNSUPPORTED;
+ *   - device_error (optional DEVICE pointer to one int32, may be NULL) receives this call's device
+ *     error word (see dsa_get_device_error) on `stream` after the kernel.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Each call clears the error word
+ * on `stream` before launching.  All calls share the one array, so calls that may overlap on the
+ * GPU (different streams, or different host threads) race on it.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine is called.
+ */
+dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, const float* q_scale,
+                                     const float* w, const void* k_cache, const float* k_scale,
+                                     const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                     int32_t* topk_idx, int32_t* device_error, void* stream);
+
+/*
  * Synchronises `stream`, then reads the device error word of `workspace` into *code (host pointer).
  * Returns DSA_OK if it is zero, DSA_ERR_TIMEOUT if DSA_DEVERR_TIMEOUT is set, DSA_ERR_DEVICE for any
  * other bit, DSA_ERR_CUDA if the synchronisation or the copy fails.

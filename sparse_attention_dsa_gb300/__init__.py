@@ -27,6 +27,7 @@ from ._lib import (  # noqa: F401
     fused_decode,
     get_device_error,
     indexer_topk,
+    indexer_topk_static,
     lib,
     sparse_attn,
     status_string,

@@ -28,6 +28,7 @@ EXPORTED = (
     "dsa_fused_decode",
     "dsa_get_device_error",
     "dsa_clear_device_error",
+    "dsa_indexer_topk_static",
 )
 
 
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
             L.dsa_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
             L.dsa_clear_device_error.restype = st
             L.dsa_clear_device_error.argtypes = [vp, vp]
+            L.dsa_indexer_topk_static.restype = st
+            L.dsa_indexer_topk_static.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 11
             _lib = L
     return _lib
 
@@ -152,6 +155,14 @@ def fused_decode(dims, q_idx, q_scale, w, k_cache, k_scale, q, kv_cache, page_ta
                                   _ptr(k_scale), _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),
                                   _ptr(cu_q_lens), _ptr(topk_idx), _ptr(out), _ptr(lse), _ptr(workspace),
                                   _stream(stream)))
+
+
+def indexer_topk_static(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx,
+                        device_error=None, stream=None):
+    """dsa_indexer_topk_static: no workspace; the library's static device scratch is used instead."""
+    _check(lib().dsa_indexer_topk_static(ctypes.byref(dims), _ptr(q_idx), _ptr(q_scale), _ptr(w), _ptr(k_cache),
+                                         _ptr(k_scale), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q_lens),
+                                         _ptr(topk_idx), _ptr(device_error), _stream(stream)))
 
 
 def get_device_error(workspace, stream=None) -> int:

@@ -301,6 +301,8 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
 
 }  // namespace
 
+void dsa::set_last_error(const char* message) { g_last_error = message ? message : ""; }
+
 extern "C" {
 
 int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }

@@ -79,4 +79,7 @@ struct SfaLaunch {
 
 cudaError_t launch_sfa(const SfaLaunch& launch, cudaStream_t stream);
 
+// Sets the message returned by dsa_last_error_message() on this host thread.
+void set_last_error(const char* message);
+
 }  // namespace dsa
