@@ -106,7 +106,7 @@ dsa_status_t check_common(const dsa_dims_t* d) {
     return DSA_OK;
 }
 
-constexpr int kKeyBudgetBytes = 64 * 1024;
+constexpr int kMaxClusterSize = 16;
 
 dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::IndexerLaunch* L) {
     if (d->idx_heads < 1 || d->idx_dim < 1)
@@ -123,29 +123,36 @@ dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::Index
     else
         return fail(DSA_ERR_UNSUPPORTED, "indexer shape (heads %d, dim %d, %s) has no kernel variant", d->idx_heads,
                     d->idx_dim, fp8 ? "fp8" : "bf16");
-    int qb = d->max_q_len < qb_max ? d->max_q_len : qb_max;
-    if (qb == 3) qb = 4;
-    const int qb_template = (d->idx_heads == 4) ? 4 : qb;  // the Hi=4 variant always reserves 4 query slots
-    if (dsa::indexer_variant_n(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, qb) == 0)
-        return fail(DSA_ERR_UNSUPPORTED, "no indexer variant for %d query tokens per block", qb);
-    const int blocks_per_seq = (d->max_q_len + qb - 1) / qb;
-    const int64_t items = (int64_t)d->batch * blocks_per_seq;
-    if (items > (1 << 26)) return fail(DSA_ERR_UNSUPPORTED, "too many work items (%lld)", (long long)items);
+    int qb_want = d->max_q_len < qb_max ? d->max_q_len : qb_max;
+    if (qb_want == 3) qb_want = 4;
     auto chunk_for = [&](int C) -> int64_t {
         const int64_t per = (max_ctx + C - 1) / C;
         return (per + 127) / 128 * 128;
     };
-    int c_min = 0;
-    for (int C = 1; C <= 16; C *= 2)
-        if (chunk_for(C) * qb_template * 4 <= kKeyBudgetBytes) {
-            c_min = C;
-            break;
+    // Largest query block (up to qb_want) and smallest cluster for which a CTA's slice of the scores fits
+    // in shared memory next to a pipeline of at least 3 stages (2 accepted as a last resort).
+    int qb = 0, c_min = 0;
+    for (int min_stages = 3; min_stages >= 2 && c_min == 0; --min_stages)
+        for (int q = qb_want; q >= 1 && c_min == 0; q /= 2) {
+            if (dsa::indexer_variant_n(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, q) == 0) continue;
+            for (int C = 1; C <= kMaxClusterSize; C *= 2)
+                if (chunk_for(C) <= INT32_MAX &&
+                    dsa::indexer_smem_estimate(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, q, min_stages, (int)chunk_for(C),
+                                               C) <= (size_t)dev.smem_optin) {
+                    qb = q;
+                    c_min = C;
+                    break;
+                }
         }
     if (c_min == 0)
-        return fail(DSA_ERR_UNSUPPORTED, "context of %lld positions with %d query tokens per block exceeds the on-chip "
-                    "score capacity (16 CTAs x %d KiB)", (long long)max_ctx, qb, kKeyBudgetBytes / 1024);
+        return fail(DSA_ERR_UNSUPPORTED, "context of %lld positions exceeds the on-chip score capacity of a %d-CTA "
+                    "cluster", (long long)max_ctx, kMaxClusterSize);
+    const int blocks_per_seq = (d->max_q_len + qb - 1) / qb;
+    const int64_t items = (int64_t)d->batch * blocks_per_seq;
+    if (items > (1 << 26)) return fail(DSA_ERR_UNSUPPORTED, "too many work items (%lld)", (long long)items);
+    // Otherwise as many CTAs per work item as keep every CTA resident (portable cluster sizes up to 8).
     int c_target = 1;
-    while (c_target < 16 && items * (c_target * 2) <= dev.num_sms) c_target *= 2;
+    while (c_target < 8 && items * (c_target * 2) <= dev.num_sms) c_target *= 2;
     const int C = c_min > c_target ? c_min : c_target;
     L->cluster = C;
     L->items = (int)items;

@@ -49,8 +49,10 @@ struct IdxCfg {
     static constexpr int kQBytes = kN * kRowBytes;
     static constexpr int kMmaK = FP8 ? 32 : 16;  // elements per UMMA
     static constexpr int kKSteps = DI / kMmaK;
-    static constexpr int kTmemCols = (2 * kN) <= 32 ? 32 : (2 * kN) <= 64 ? 64 : (2 * kN) <= 128 ? 128
-                                                                                 : (2 * kN) <= 256 ? 256 : 512;
+    // accumulator buffers in TMEM: enough that the MMA issuer rarely waits for the epilogue
+    static constexpr int kAccBufs = (4 * kN) <= 512 ? 4 : 2;
+    static constexpr int kTmemCols = (kAccBufs * kN) <= 32 ? 32 : (kAccBufs * kN) <= 64 ? 64
+                                     : (kAccBufs * kN) <= 128 ? 128 : (kAccBufs * kN) <= 256 ? 256 : 512;
     static constexpr uint32_t kIdesc = make_idesc(128, kN, FP8 ? 0u : 1u, FP8 ? 0u : 1u, 0u, 0u);
     static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
     static_assert(kN <= 256, "UMMA N limit");
@@ -72,8 +74,8 @@ struct SelectSmem {
 struct CtrlSmem {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tfull[4];
+    uint64_t tempty[4];
     uint64_t qbar;
     uint32_t tmem_base;
     int32_t consumed;  // tiles consumed by the MMA warp (drain bookkeeping)
@@ -107,6 +109,7 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         const int shift = 24 - 8 * pass;
         const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
         const int buf = pass & 1;
+        uint32_t* ah = allh + buf * C * 256;  // this pass's gathered histograms, [C][256]
         if (pass > 0) {  // the top-byte histogram (pass 0) was built while scoring
             S.hist[buf][tid] = 0;
             __syncthreads();
@@ -118,16 +121,19 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
                     if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[buf][bin], (uint32_t)__popc(peers));
                 }
             }
+            __syncthreads();
+        }
+        {
+            // push this CTA's bin count into slot [rank] of every CTA's buffer (posted remote stores);
+            // the cluster barrier below makes them visible
+            const uint32_t v = pass == 0 ? hist0[tid] : S.hist[buf][tid];
+            const uint32_t slot = smem_u32(ah + rank * 256 + tid);
+            for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), v);
         }
         cluster_sync();
         {
             uint32_t tot = 0;
-            const uint32_t local = pass == 0 ? smem_u32(hist0 + tid) : smem_u32(&S.hist[buf][tid]);
-            for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t v = ld_dsmem_u32(mapa_shared(local, r));
-                allh[r * 256 + tid] = v;
-                tot += v;
-            }
+            for (uint32_t r = 0; r < C; ++r) tot += ah[r * 256 + tid];
             S.totals[tid] = tot;
         }
         __syncthreads();
@@ -158,12 +164,12 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         const uint32_t bstar = S.bstar;
         for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
             uint32_t s = 0;
-            for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? allh[r * 256 + i] : 0u;
+            for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? ah[r * 256 + i] : 0u;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
             if (lane == 0) S.gt[r] += s;
         }
-        if (pass == 3 && tid < (int)C) S.ecnt[tid] = allh[tid * 256 + bstar];
+        if (pass == 3 && tid < (int)C) S.ecnt[tid] = ah[tid * 256 + bstar];
         remaining = S.remaining;
         prefix |= bstar << shift;
         __syncthreads();
@@ -184,35 +190,44 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     }
     __syncthreads();
     const uint32_t take_me = S.take_me, off_me = S.off_me;
-    uint32_t run_tie = 0, run_sel = 0;
+    // Ordered compaction.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of the local keys:
+    // one pass counts its keys above T and its ties, a block barrier turns the counts into per-warp
+    // offsets, a second pass writes the selected positions in order.
     const int nw = kThreads / 32;
-    for (int base = 0; base < n; base += kThreads) {
-        const int i = base + tid;
-        const uint32_t key = i < n ? keys[i] : 0u;
-        const bool e = key == T, g = key > T;
+    const int seg = ((n + nw - 1) / nw + 31) / 32 * 32;
+    const int lo = warp * seg, hi = min(n, lo + seg);
+    uint32_t cnt_gt = 0, cnt_tie = 0;
+    for (int base = lo; base < hi; base += 32) {
+        const int i = base + lane;
+        const uint32_t key = i < hi ? keys[i] : 0u;
+        cnt_gt += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, key > T));
+        cnt_tie += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, key == T && i < hi));
+    }
+    if (lane == 0) {
+        S.scan_e[warp] = cnt_tie;
+        S.scan_s[warp] = cnt_gt;
+    }
+    __syncthreads();
+    uint32_t tie_base = 0, out_base = off_me;
+    for (int k = 0; k < warp; ++k) {
+        const uint32_t ties_k = S.scan_e[k];
+        const uint32_t take_k = take_me > tie_base ? min(ties_k, take_me - tie_base) : 0u;
+        out_base += S.scan_s[k] + take_k;
+        tie_base += ties_k;
+    }
+    if (cnt_gt == 0 && (cnt_tie == 0 || tie_base >= take_me)) return;  // nothing selected in this segment
+    uint32_t run_tie = tie_base, run_sel = 0;
+    for (int base = lo; base < hi; base += 32) {
+        const int i = base + lane;
+        const uint32_t key = i < hi ? keys[i] : 0u;
+        const bool e = key == T && i < hi, g = key > T;
         const uint32_t be = __ballot_sync(0xFFFFFFFFu, e);
-        if (lane == 0) S.scan_e[warp] = (uint32_t)__popc(be);
-        __syncthreads();
-        uint32_t wpre = 0, wtot = 0;
-        for (int k = 0; k < nw; ++k) {
-            const uint32_t c = S.scan_e[k];
-            wpre += k < warp ? c : 0u;
-            wtot += c;
-        }
-        const uint32_t tie_rank = run_tie + wpre + (uint32_t)__popc(be & lanemask_lt());
+        const uint32_t tie_rank = run_tie + (uint32_t)__popc(be & lanemask_lt());
         const bool sel = g || (e && tie_rank < take_me);
         const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
-        if (lane == 0) S.scan_s[warp] = (uint32_t)__popc(bs);
-        __syncthreads();
-        uint32_t spre = 0, stot = 0;
-        for (int k = 0; k < nw; ++k) {
-            const uint32_t c = S.scan_s[k];
-            spre += k < warp ? c : 0u;
-            stot += c;
-        }
-        if (sel) out_row[off_me + run_sel + spre + (uint32_t)__popc(bs & lanemask_lt())] = range_start + i;
-        run_tie += wtot;
-        run_sel += stot;
+        if (sel) out_row[out_base + run_sel + (uint32_t)__popc(bs & lanemask_lt())] = range_start + i;
+        run_tie += (uint32_t)__popc(be);
+        run_sel += (uint32_t)__popc(bs);
     }
 }
 
@@ -231,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
     int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + p.chunk / kPage);  // QB x 256
-    uint32_t* allh = hist0 + QB * 256;                                      // C x 256
-    SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + cluster_nctarank() * 256);
+    uint32_t* allh = hist0 + QB * 256;                                      // 2 x C x 256
+    SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + 2 * cluster_nctarank() * 256);
     CtrlSmem* ctl = reinterpret_cast<CtrlSmem*>((reinterpret_cast<uintptr_t>(sel + 1) + 15) & ~uintptr_t(15));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -294,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
             mbar_init(&ctl->tempty[i], 4);
         }
@@ -371,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; ok && i < ntiles; ++i) {
                     const int s = i % S;
                     const uint32_t ph = (uint32_t)(i / S) & 1u;
-                    const int ab = i & 1;
-                    const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+                    const int ab = i % Cfg::kAccBufs;
+                    const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
                     if (!mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err)) break;
                     if (!mbar_wait(&ctl->full[s], ph, p.err)) break;
                     consumed = i + 1;
@@ -402,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < QB; ++q) pq[q] = (int64_t)L - n_b + j0 + q;
             for (int i = 0; i < ntiles; ++i) {
-                const int ab = i & 1;
-                const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+                const int ab = i % Cfg::kAccBufs;
+                const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
                 const int local = i * kTileM + row;
                 const int pos = range_start + local;
                 const int32_t pg = pages_s[2 * i + (row >> 6)];
@@ -474,7 +489,7 @@ template <int HI, int DI, int QB, bool FP8>
 size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
     using Cfg = IdxCfg<HI, DI, QB, FP8>;
     return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
-           (size_t)(chunk / kPage) * 4 + (size_t)(QB + cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
+           (size_t)(chunk / kPage) * 4 + (size_t)(QB + 2 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
            64;
 }
 
@@ -522,6 +537,21 @@ int indexer_variant_n(int idx_heads, int idx_dim, int fp8, int qb) {
     if (!fp8 && idx_heads == 4 && idx_dim == 64 && qb >= 1 && qb <= 4) return 16;
     if (idx_heads == 64 && idx_dim == 128 && (qb == 1 || qb == 2 || (qb == 4 && !fp8))) return 64 * qb;
     return 0;
+}
+
+size_t indexer_smem_estimate(int idx_heads, int idx_dim, int fp8, int qb, int stages, int chunk, int cluster) {
+    if (!fp8 && idx_heads == 4 && idx_dim == 64) return indexer_smem_bytes<4, 64, 4, false>(stages, chunk, cluster);
+    if (idx_heads == 64 && idx_dim == 128) {
+        if (fp8) {
+            if (qb == 1) return indexer_smem_bytes<64, 128, 1, true>(stages, chunk, cluster);
+            if (qb == 2) return indexer_smem_bytes<64, 128, 2, true>(stages, chunk, cluster);
+        } else {
+            if (qb == 1) return indexer_smem_bytes<64, 128, 1, false>(stages, chunk, cluster);
+            if (qb == 2) return indexer_smem_bytes<64, 128, 2, false>(stages, chunk, cluster);
+            if (qb == 4) return indexer_smem_bytes<64, 128, 4, false>(stages, chunk, cluster);
+        }
+    }
+    return ~size_t(0);
 }
 
 cudaError_t launch_indexer(const IndexerLaunch& L, cudaStream_t stream) {

@@ -45,6 +45,8 @@ struct IndexerLaunch {
 
 // UMMA N of the kernel variant serving (Hi, Di, dtype, qb), 0 when no variant exists.
 int indexer_variant_n(int idx_heads, int idx_dim, int fp8, int qb);
+// Dynamic shared memory of that variant for the given pipeline depth, positions per CTA and cluster size.
+size_t indexer_smem_estimate(int idx_heads, int idx_dim, int fp8, int qb, int stages, int chunk, int cluster);
 cudaError_t launch_indexer(const IndexerLaunch& launch, cudaStream_t stream);
 
 // ---- sparse flash attention --------------------------------------------------------------------------

@@ -12,13 +12,18 @@
 //   * the 128 query heads are the UMMA M dimension; Q[t] (128 x 576 bf16, 144 KiB) stays in smem;
 //   * at start every thread helps translate the split's selected positions (Top-K entry -> page table
 //     -> physical row) into a row list in smem, so no global lookup sits on the per-tile path;
-//   * two gather warps copy the selected rows 32 at a time (cp.async, 16-byte pieces written straight
-//     into the 128B-swizzled operand layout) into a 2-stage ring, and prefetch rows a few tiles ahead
-//     into L2 (cp.async.bulk.prefetch) to keep more bytes in flight than the ring holds;
-//   * S = Q K^T (M=128, N=32, K=576) lands in TMEM; softmax warps (one thread per head row) turn it into
-//     P (bf16) stored back into TMEM, with an online max that is only raised when it grows by more than
-//     2^8 (so O rarely needs rescaling);
-//   * O += P V (M=128, N=256, K=32; A = P from TMEM, B = the same smem rows read as MN-major V)
+//   * the selected rows are processed 64 at a time (UMMA N = 64: below that a tcgen05.mma costs about
+//     as much as at N = 64).  One tile buffer (64 x 576 bf16) is split into the 256 value dims this CTA
+//     owns (the "V part") and the other 320 dims (the "K part"); two gather warps refill them
+//     independently with cp.async pieces written straight into the 128B-swizzled operand layout, and
+//     prefetch rows a few tiles ahead into L2 (cp.async.bulk.prefetch);
+//   * the MMA issuer runs  QK_K(i+1) -> PV(i) -> QK_V(i+1):  S(i+1) over the K part can start as soon as
+//     that part is loaded, while the V part of tile i+1 is loaded as soon as P(i) V(i) has consumed the
+//     V part of tile i;
+//   * S lands in TMEM (two buffers); softmax warps (one thread per head row) turn it into P (bf16,
+//     stored back into TMEM, two buffers) with an online max that is only raised when it grows by more
+//     than 2^8 (so O rarely needs rescaling);
+//   * O += P V (M=128, N=256, K=64; A = P from TMEM, B = the V part read as an MN-major operand)
 //     accumulates in TMEM.  The 512 value dims are split between the two CTAs of the pair (each owns 256
 //     columns of O) because a full 128 x 512 fp32 O would fill all of TMEM; both CTAs compute the same S.
 //   * With more than one position split, the partial (O, max, sum) of the splits are merged through
@@ -34,35 +39,37 @@ namespace {
 
 constexpr int kDim = 576;  // latent + rope
 constexpr int kVDim = 512;
-constexpr int kThreadsSfa = 224;  // warp 0/6: gather (even/odd tiles), 1: MMA, 2-5: softmax
-constexpr int kRows = 32;         // selected rows per tile
+constexpr int kThreadsSfa = 224;  // warp 0: K-part gather, 6: V-part gather, 1: MMA, 2-5: softmax
+constexpr int kRows = 64;         // selected rows per tile
+constexpr int kAtoms = kDim / 64;  // 128-byte swizzle atoms per row
+constexpr int kAtomBytes = kRows * 128;
 constexpr int kQBytes = 128 * kDim * 2;
-constexpr int kKvStage = kRows * kDim * 2;
+constexpr int kTileBytes = kAtoms * kAtomBytes;
 constexpr int kMaxEntries = 2048;  // selected entries per CTA (per position split)
 constexpr int kOCols = 256;
-constexpr int kSCol = 256;  // two S buffers of 32 columns
-constexpr int kPCol = 320;  // P: 32 bf16 per row = 16 columns
+constexpr int kSCol = 256;  // two S buffers of 64 columns
+constexpr int kPCol = 384;  // two P buffers: 64 bf16 per row = 32 columns each
 constexpr int kTmemCols = 512;
-constexpr int kPrefetchTiles = 4;  // L2 prefetch distance, in tiles of the same gather warp
+constexpr int kPrefetchTiles = 2;  // L2 prefetch distance, in tiles
 constexpr uint32_t kIdescQK = make_idesc(128, kRows, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = make_idesc(128, kOCols, 1, 1, 0, 1);
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only when it grows by more than this
 
 struct SfaCtrl {
     uint64_t q_full;
-    uint64_t kv_full[2];
-    uint64_t kv_empty[2];
+    uint64_t k_full, k_empty;  // K part of the tile buffer
+    uint64_t v_full, v_empty;  // V part of the tile buffer
     uint64_t s_full[2];
     uint64_t s_empty[2];
-    uint64_t p_full;
-    uint64_t p_empty;
+    uint64_t p_full[2];
+    uint64_t p_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t q_waited;
     float2 ml[128];
 };
 
-constexpr size_t kSfaSmem = 1024 + kQBytes + 2 * kKvStage + kMaxEntries * 4 + sizeof(SfaCtrl);
+constexpr size_t kSfaSmem = 1024 + kQBytes + kTileBytes + kMaxEntries * 4 + sizeof(SfaCtrl);
 
 __device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
     // round to nearest even (finite inputs); a in the low half
@@ -82,7 +89,7 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
         "%14, %15, %16};" ::"r"(taddr),
@@ -95,13 +102,16 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Atom a (64 dims) of a row belongs to the V part of the CTA that owns value half dvh.
+__device__ __forceinline__ bool is_v_atom(int a, int dvh) { return a >= 4 * dvh && a < 4 * dvh + 4; }
+
 __global__ void __launch_bounds__(kThreadsSfa, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q_s = smem;
-    uint8_t* kv_s = q_s + kQBytes;
-    int32_t* rows_s = reinterpret_cast<int32_t*>(kv_s + 2 * kKvStage);  // physical row per entry, -1 = skip
+    uint8_t* kv_s = q_s + kQBytes;                                   // [atom][64 rows][128 B]
+    int32_t* rows_s = reinterpret_cast<int32_t*>(kv_s + kTileBytes);  // physical row per entry, -1 = skip
     SfaCtrl* ctl = reinterpret_cast<SfaCtrl*>(rows_s + kMaxEntries);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -158,14 +168,16 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     }
     if (tid == 0) {
         mbar_init(&ctl->q_full, 1);
+        mbar_init(&ctl->k_full, 1);
+        mbar_init(&ctl->k_empty, 1);
+        mbar_init(&ctl->v_full, 1);
+        mbar_init(&ctl->v_empty, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl->kv_full[i], 1);
-            mbar_init(&ctl->kv_empty[i], 1);
             mbar_init(&ctl->s_full[i], 1);
             mbar_init(&ctl->s_empty[i], 4);
+            mbar_init(&ctl->p_full[i], 4);
+            mbar_init(&ctl->p_empty[i], 1);
         }
-        mbar_init(&ctl->p_full, 4);
-        mbar_init(&ctl->p_empty, 1);
         mbar_init(&ctl->mma_done, 1);
         ctl->q_waited = 0;
         fence_mbar_init();
@@ -181,36 +193,43 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
 
     float m_used = -INFINITY, l_sum = 0.f;  // softmax threads: running max (log2 units) and sum
     if (warp == 0 || warp == 6) {
-        // ---------------- gather: warp 0 fills even tiles (stage 0), warp 6 odd tiles (stage 1) ----------------
-        const int par = warp == 0 ? 0 : 1;
+        // ---------------- gather: warp 0 fills the K part, warp 6 the V part ----------------
+        const bool v_part = warp == 6;
+        uint64_t* full = v_part ? &ctl->v_full : &ctl->k_full;
+        uint64_t* empty = v_part ? &ctl->v_empty : &ctl->k_empty;
         if (warp == 0 && lane == 0) {
             prefetch_tensormap(&qmap);
             mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
-            for (int a = 0; a < kDim / 64; ++a) tma_load_2d(q_s + a * (128 * 128), &qmap, &ctl->q_full, a * 64, t * p.heads);
+            for (int a = 0; a < kAtoms; ++a) tma_load_2d(q_s + a * (128 * 128), &qmap, &ctl->q_full, a * 64, t * p.heads);
         }
-        // warm L2 with this warp's first tiles
-        for (int i = par; i < ntiles && i < par + 2 * kPrefetchTiles; i += 2) {
-            const int32_t row = rows_s[i * kRows + lane];
-            if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
-        }
-        uint8_t* stage = kv_s + par * kKvStage;
-        for (int i = par; i < ntiles; i += 2) {
-            const int ahead = i + 2 * kPrefetchTiles;
-            if (ahead < ntiles) {
-                const int32_t row = rows_s[ahead * kRows + lane];
+        if (!v_part) {  // warm L2 with the first tiles
+            for (int e = lane; e < kPrefetchTiles * kRows && e < ntiles * kRows; e += 32) {
+                const int32_t row = rows_s[e];
                 if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
             }
-            if (!mbar_wait(&ctl->kv_empty[par], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err)) break;
+        }
+        for (int i = 0; i < ntiles; ++i) {
+            if (!v_part) {
+                const int ahead = i + kPrefetchTiles;
+                if (ahead < ntiles) {
+                    for (int e = lane; e < kRows; e += 32) {
+                        const int32_t row = rows_s[ahead * kRows + e];
+                        if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
+                    }
+                }
+            }
+            if (!mbar_wait(empty, ((uint32_t)i & 1u) ^ 1u, p.err)) break;
+            const int c8 = lane & 7;
 #pragma unroll 1
             for (int r0 = 0; r0 < kRows; r0 += 4) {
                 const int r = r0 + (lane >> 3);
-                const int c8 = lane & 7;
                 const int32_t row = rows_s[i * kRows + r];
                 const uint16_t* src = p.kv_cache + (int64_t)row * kDim + c8 * 8;
-                const uint32_t row_base = smem_u32(stage) + r * 128 + ((c8 ^ (r & 7)) << 4);
+                const uint32_t row_base = smem_u32(kv_s) + r * 128 + ((c8 ^ (r & 7)) << 4);
 #pragma unroll
-                for (int a = 0; a < kDim / 64; ++a) {
-                    const uint32_t dst = row_base + a * (kRows * 128);
+                for (int a = 0; a < kAtoms; ++a) {
+                    if (is_v_atom(a, dvh) != v_part) continue;
+                    const uint32_t dst = row_base + a * kAtomBytes;
                     if (row >= 0)
                         cp_async_16(dst, src + a * 64);
                     else
@@ -221,49 +240,62 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
             cp_async_wait_group<0>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->kv_full[par]);
+            if (lane == 0) mbar_arrive(full);
         }
         cp_async_wait_group<0>();
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- MMA issuer: QK_K(i+1) -> PV(i) -> QK_V(i+1) ----------------
         if (lane == 0) {
             bool ok = mbar_wait(&ctl->q_full, 0, p.err);
             ctl->q_waited = ok ? 1 : 0;
             const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s);
-            auto issue_qk = [&](int j) -> bool {
-                const int st = j & 1;
-                const uint32_t ph = ((uint32_t)j >> 1) & 1u;
-                if (!mbar_wait(&ctl->kv_full[st], ph, p.err)) return false;
-                if (!mbar_wait(&ctl->s_empty[st], ph ^ 1u, p.err)) return false;
-                tc_fence_after();
+            // S(j) over the atoms of one part; the first MMA of the K part overwrites the accumulator
+            auto issue_qk_part = [&](int j, bool v_part) {
+                const uint32_t d = tmem + kSCol + (j & 1) * kRows;
+                bool first = !v_part;
 #pragma unroll
-                for (int a = 0; a < kDim / 64; ++a) {
+                for (int a = 0; a < kAtoms; ++a) {
+                    if (is_v_atom(a, dvh) != v_part) continue;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc(q_base + a * (128 * 128) + kk * 32, 16, 1024, kSwizzle128B);
-                        const uint64_t bd =
-                            smem_desc(kv_base + st * kKvStage + a * (kRows * 128) + kk * 32, 16, 1024, kSwizzle128B);
-                        umma_f16_ss(tmem + kSCol + st * kRows, ad, bd, kIdescQK, (a | kk) != 0);
+                        const uint64_t bd = smem_desc(kv_base + a * kAtomBytes + kk * 32, 16, 1024, kSwizzle128B);
+                        umma_f16_ss(d, ad, bd, kIdescQK, first ? 0u : 1u);
+                        first = false;
                     }
                 }
-                umma_commit(&ctl->s_full[st]);
+            };
+            auto qk_k = [&](int j) -> bool {  // needs the K part of tile j and a free S buffer
+                if (!mbar_wait(&ctl->k_full, (uint32_t)j & 1u, p.err)) return false;
+                if (!mbar_wait(&ctl->s_empty[j & 1], (((uint32_t)j >> 1) & 1u) ^ 1u, p.err)) return false;
+                tc_fence_after();
+                issue_qk_part(j, false);
+                umma_commit(&ctl->k_empty);
                 return true;
             };
-            if (ok && ntiles > 0) ok = issue_qk(0);
-            for (int i = 0; ok && i < ntiles; ++i) {
-                if (i + 1 < ntiles && !issue_qk(i + 1)) break;
-                if (!mbar_wait(&ctl->p_full, (uint32_t)i & 1u, p.err)) break;
+            auto qk_v = [&](int j) -> bool {  // needs the V part of tile j
+                if (!mbar_wait(&ctl->v_full, (uint32_t)j & 1u, p.err)) return false;
                 tc_fence_after();
-                const int st = i & 1;
+                issue_qk_part(j, true);
+                umma_commit(&ctl->s_full[j & 1]);
+                return true;
+            };
+            if (ok && ntiles > 0) ok = qk_k(0) && qk_v(0);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                if (i + 1 < ntiles && !qk_k(i + 1)) break;
+                if (!mbar_wait(&ctl->p_full[i & 1], ((uint32_t)i >> 1) & 1u, p.err)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kRows / 16; ++kk) {
-                    // V rows of this stage as an MN-major operand: 64-dim atoms 4096 B apart, 8-row groups 1024 B
-                    const uint64_t bd = smem_desc(kv_base + st * kKvStage + (dvh * 4) * (kRows * 128) + kk * 2048,
-                                                  kRows * 128, 1024, kSwizzle128B);
-                    umma_f16_ts(tmem, tmem + kPCol + kk * 8, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    // V part as an MN-major operand: 64-dim atoms kAtomBytes apart, 8-row groups 1024 B apart
+                    const uint64_t bd = smem_desc(kv_base + (dvh * 4) * kAtomBytes + kk * 2048, kAtomBytes, 1024,
+                                                  kSwizzle128B);
+                    umma_f16_ts(tmem, tmem + kPCol + (i & 1) * (kRows / 2) + kk * 8, bd, kIdescPV,
+                                (i > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(&ctl->kv_empty[st]);
-                umma_commit(&ctl->p_empty);
+                umma_commit(&ctl->v_empty);
+                umma_commit(&ctl->p_empty[i & 1]);
+                if (i + 1 < ntiles && !qk_v(i + 1)) break;
             }
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, p.err);
@@ -273,38 +305,40 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t trow = tmem + ((quad * 32u) << 16);
         for (int i = 0; i < ntiles; ++i) {
-            const int st = i & 1;
-            const uint32_t vmask = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
-            if (!mbar_wait(&ctl->s_full[st], ((uint32_t)i >> 1) & 1u, p.err)) break;
+            const int sb = i & 1;
+            const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
+            const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + 32 + lane] >= 0);
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full[sb], ((uint32_t)i >> 1) & 1u, p.err))) break;
             tc_fence_after();
-            float sv[32];
-            {
-                float a0[16], a1[16];
-                tmem_ld16(trow + kSCol + st * kRows, a0);
-                tmem_ld16(trow + kSCol + st * kRows + 16, a1);
+            float sv[kRows];
+#pragma unroll
+            for (int c = 0; c < kRows / 16; ++c) {
+                float a16[16];
+                tmem_ld16(trow + kSCol + sb * kRows + c * 16, a16);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    sv[j] = a0[j];
-                    sv[16 + j] = a1[j];
-                }
+                for (int j = 0; j < 16; ++j) sv[c * 16 + j] = a16[j];
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->s_empty[st]);
+            if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
             float mt = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
-                sv[j] = ((vmask >> j) & 1u) ? sv[j] * p.scale_log2 : -INFINITY;
+                const uint32_t m = j < 32 ? vm0 : vm1;
+                sv[j] = ((m >> (j & 31)) & 1u) ? sv[j] * p.scale_log2 : -INFINITY;
                 mt = fmaxf(mt, sv[j]);
             }
             const bool raise = mt > m_used + kRescaleLog2;
             const float m_new = raise ? mt : m_used;
-            // O and the P columns are free once the previous P.V has completed
-            if (!mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) break;
-            tc_fence_after();
             const float alpha = (raise && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
+            // the P buffer of this tile is free once P(i-2) V(i-2) has completed
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty[sb], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
             if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+                // rescaling O needs every earlier P V to have completed (i >= 1 here, since m_used was finite)
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty[sb ^ 1], ((uint32_t)(i - 1) >> 1) & 1u, p.err)))
+                    break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < kOCols / 16; ++c) {
                     float o[16];
@@ -315,9 +349,10 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                     tmem_st16(trow + c * 16, o);
                 }
             }
+            tc_fence_after();
             l_sum *= alpha;
             m_used = m_new;
-            uint32_t packed[16];
+            uint32_t packed[kRows / 2];
             float rs = 0.f;
 #pragma unroll
             for (int j = 0; j < kRows; j += 2) {
@@ -328,13 +363,14 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 rs += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
             }
             l_sum += rs;
-            tmem_st16_u32(trow + kPCol, packed);
+            tmem_st16_u32(trow + kPCol + sb * (kRows / 2), packed);
+            tmem_st16_u32(trow + kPCol + sb * (kRows / 2) + 16, packed + 16);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->p_full);
+            if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
         }
-        if (ntiles > 0) mbar_wait(&ctl->p_empty, ((uint32_t)(ntiles - 1)) & 1u, p.err);
+        if (ntiles > 0) mbar_wait(&ctl->p_empty[(ntiles - 1) & 1], ((uint32_t)(ntiles - 1) >> 1) & 1u, p.err);
         tc_fence_after();
     }
     tc_fence_before();
