@@ -435,6 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld16(tmem + ab * Cfg::kN + c0, v0);
                     if (c0 + 16 < Cfg::kNReal) tmem_ld16(tmem + ab * Cfg::kN + c0 + 16, v1);
                     tmem_ld_wait();
+                    tmem_regs_ready(v0);
+                    if (c0 + 16 < Cfg::kNReal) tmem_regs_ready(v1);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int c = c0 + j;

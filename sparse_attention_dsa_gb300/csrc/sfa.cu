@@ -9,20 +9,20 @@
 // the computation on the current ones).
 //
 // One CTA pair per (query token, position split):
-//   * the 128 query heads are the UMMA M dimension; Q[t] (128 x 576 bf16, 144 KiB) stays in smem;
+//   * the 128 query heads are the UMMA M dimension.  Q[t] (128 x 576 bf16) is split by 64-dim atoms:
+//     atoms 0-3 stay in shared memory (SMEM A operand), atoms 4-8 live in tensor memory (TMEM A
+//     operand), which leaves shared memory for double-buffered row tiles;
 //   * at start every thread helps translate the split's selected positions (Top-K entry -> page table
 //     -> physical row) into a row list in smem, so no global lookup sits on the per-tile path;
 //   * the selected rows are processed 64 at a time (UMMA N = 64: below that a tcgen05.mma costs about
-//     as much as at N = 64).  One tile buffer (64 x 576 bf16) is split into the 256 value dims this CTA
-//     owns (the "V part") and the other 320 dims (the "K part"); two gather warps refill them
-//     independently with cp.async pieces written straight into the 128B-swizzled operand layout, and
-//     prefetch rows a few tiles ahead into L2 (cp.async.bulk.prefetch);
-//   * the MMA issuer runs  QK_K(i+1) -> PV(i) -> QK_V(i+1):  S(i+1) over the K part can start as soon as
-//     that part is loaded, while the V part of tile i+1 is loaded as soon as P(i) V(i) has consumed the
-//     V part of tile i;
-//   * S lands in TMEM (two buffers); softmax warps (one thread per head row) turn it into P (bf16,
-//     stored back into TMEM, two buffers) with an online max that is only raised when it grows by more
-//     than 2^8 (so O rarely needs rescaling);
+//     as much as at N = 64).  Each tile is kept as the 256 value dims this CTA owns (the "V part") and
+//     the other 320 dims (the "K part"), each double-buffered.  Two pairs of gather warps refill them
+//     with cp.async pieces written straight into the 128B-swizzled operand layout (per-lane 16-byte
+//     copies issue faster here than TMA tile::gather4, which moves only 4 rows per copy) and prefetch
+//     rows a few tiles ahead into L2 (cp.async.bulk.prefetch);
+//   * the MMA issuer runs S(i) = Q K(i)^T, then O += P(i-1) V(i-1); the softmax of tile i (one thread per
+//     head row, online max raised only when it grows by more than 2^8 so O rarely needs rescaling)
+//     overlaps S(i+1) on the tensor pipe;
 //   * O += P V (M=128, N=256, K=64; A = P from TMEM, B = the V part read as an MN-major operand)
 //     accumulates in TMEM.  The 512 value dims are split between the two CTAs of the pair (each owns 256
 //     columns of O) because a full 128 x 512 fp32 O would fill all of TMEM; both CTAs compute the same S.
@@ -39,44 +39,48 @@ namespace {
 
 constexpr int kDim = 576;  // latent + rope
 constexpr int kVDim = 512;
-constexpr int kThreadsSfa = 224;  // warp 0: K-part gather, 6: V-part gather, 1: MMA, 2-5: softmax
+constexpr int kThreadsSfa = 288;  // warps 0/7: K-part gather, 6/8: V-part gather, 1: MMA, 2-5: softmax
 constexpr int kRows = 64;         // selected rows per tile
 constexpr int kAtoms = kDim / 64;  // 128-byte swizzle atoms per row
+constexpr int kSmemQAtoms = 4;     // Q atoms 0-3 in smem, 4-8 in TMEM
+constexpr int kKAtoms = 5;         // atoms of the K part (the V part has 4)
 constexpr int kAtomBytes = kRows * 128;
-constexpr int kQBytes = 128 * kDim * 2;
-constexpr int kTileBytes = kAtoms * kAtomBytes;
+constexpr int kQAtomBytes = 128 * 128;
+constexpr int kQBytes = kSmemQAtoms * kQAtomBytes;
+constexpr int kKBufBytes = kKAtoms * kAtomBytes;
+constexpr int kVBufBytes = 4 * kAtomBytes;
 constexpr int kMaxEntries = 2048;  // selected entries per CTA (per position split)
-constexpr int kOCols = 256;
-constexpr int kSCol = 256;  // two S buffers of 64 columns
-constexpr int kPCol = 384;  // two P buffers: 64 bf16 per row = 32 columns each
+constexpr int kOCols = 256;        // TMEM columns [0, 256): O (this CTA's value half)
+constexpr int kSCol = 256;         // [256, 320): S
+constexpr int kPCol = 320;         // [320, 352): P, 64 bf16 per row
+constexpr int kQCol = 352;         // [352, 512): Q atoms 4-8, 32 columns each
 constexpr int kTmemCols = 512;
-constexpr int kPrefetchTiles = 2;  // L2 prefetch distance, in tiles
+constexpr int kPrefetchTiles = 3;  // L2 prefetch distance, in tiles
 constexpr uint32_t kIdescQK = make_idesc(128, kRows, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = make_idesc(128, kOCols, 1, 1, 0, 1);
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only when it grows by more than this
 
 struct SfaCtrl {
-    uint64_t q_full;
-    uint64_t k_full, k_empty;  // K part of the tile buffer
-    uint64_t v_full, v_empty;  // V part of the tile buffer
-    uint64_t s_full[2];
-    uint64_t s_empty[2];
-    uint64_t p_full[2];
-    uint64_t p_empty[2];
+    uint64_t q_full;   // Q atoms 0-3 in smem
+    uint64_t qt_full;  // Q atoms 4-8 in TMEM
+    uint64_t k_full[2], k_empty[2];
+    uint64_t v_full[2], v_empty[2];
+    uint64_t s_full, s_empty;
+    uint64_t p_full, p_empty;
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t q_waited;
     float2 ml[128];
 };
 
-constexpr size_t kSfaSmem = 1024 + kQBytes + kTileBytes + kMaxEntries * 4 + sizeof(SfaCtrl);
+constexpr size_t kSfaSmem =
+    1024 + kQBytes + 2 * kKBufBytes + 2 * kVBufBytes + kMaxEntries * 4 + sizeof(SfaCtrl);
 
+// bf16 pair, round to nearest even; a in the low half
 __device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
-    // round to nearest even (finite inputs); a in the low half
-    uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
-    ua += 0x7FFFu + ((ua >> 16) & 1u);
-    ub += 0x7FFFu + ((ub >> 16) & 1u);
-    return (ua >> 16) | (ub & 0xFFFF0000u);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs.
@@ -104,14 +108,20 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 
 // Atom a (64 dims) of a row belongs to the V part of the CTA that owns value half dvh.
 __device__ __forceinline__ bool is_v_atom(int a, int dvh) { return a >= 4 * dvh && a < 4 * dvh + 4; }
+// Slot of atom a inside its part's buffer.
+__device__ __forceinline__ int part_slot(int a, int dvh) {
+    if (is_v_atom(a, dvh)) return a - 4 * dvh;
+    return dvh == 0 ? a - 4 : (a < 4 ? a : 4);
+}
 
 __global__ void __launch_bounds__(kThreadsSfa, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* q_s = smem;
-    uint8_t* kv_s = q_s + kQBytes;                                   // [atom][64 rows][128 B]
-    int32_t* rows_s = reinterpret_cast<int32_t*>(kv_s + kTileBytes);  // physical row per entry, -1 = skip
+    uint8_t* q_s = smem;                         // Q atoms 0-3: [atom][128 rows][128 B]
+    uint8_t* kbuf = q_s + kQBytes;               // 2 x K part: [slot][64 rows][128 B]
+    uint8_t* vbuf = kbuf + 2 * kKBufBytes;       // 2 x V part
+    int32_t* rows_s = reinterpret_cast<int32_t*>(vbuf + 2 * kVBufBytes);  // physical row per entry, -1 = skip
     SfaCtrl* ctl = reinterpret_cast<SfaCtrl*>(rows_s + kMaxEntries);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -168,16 +178,17 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     }
     if (tid == 0) {
         mbar_init(&ctl->q_full, 1);
-        mbar_init(&ctl->k_full, 1);
-        mbar_init(&ctl->k_empty, 1);
-        mbar_init(&ctl->v_full, 1);
-        mbar_init(&ctl->v_empty, 1);
+        mbar_init(&ctl->qt_full, 4);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl->s_full[i], 1);
-            mbar_init(&ctl->s_empty[i], 4);
-            mbar_init(&ctl->p_full[i], 4);
-            mbar_init(&ctl->p_empty[i], 1);
+            mbar_init(&ctl->k_full[i], 64);  // one cp.async-tracked arrival per gather lane
+            mbar_init(&ctl->k_empty[i], 1);
+            mbar_init(&ctl->v_full[i], 64);
+            mbar_init(&ctl->v_empty[i], 1);
         }
+        mbar_init(&ctl->s_full, 1);
+        mbar_init(&ctl->s_empty, 4);
+        mbar_init(&ctl->p_full, 4);
+        mbar_init(&ctl->p_empty, 1);
         mbar_init(&ctl->mma_done, 1);
         ctl->q_waited = 0;
         fence_mbar_init();
@@ -192,24 +203,25 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     const uint32_t tmem = ctl->tmem_base;
 
     float m_used = -INFINITY, l_sum = 0.f;  // softmax threads: running max (log2 units) and sum
-    if (warp == 0 || warp == 6) {
-        // ---------------- gather: warp 0 fills the K part, warp 6 the V part ----------------
-        const bool v_part = warp == 6;
-        uint64_t* full = v_part ? &ctl->v_full : &ctl->k_full;
-        uint64_t* empty = v_part ? &ctl->v_empty : &ctl->k_empty;
+    if (warp == 0 || warp >= 6) {
+        // ---------------- gather: warps 0/7 fill the K part, warps 6/8 the V part, 32 rows each ----------------
+        const bool v_part = warp == 6 || warp == 8;
+        const int row0 = (warp == 7 || warp == 8) ? kRows / 2 : 0;
         if (warp == 0 && lane == 0) {
             prefetch_tensormap(&qmap);
             mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
-            for (int a = 0; a < kAtoms; ++a) tma_load_2d(q_s + a * (128 * 128), &qmap, &ctl->q_full, a * 64, t * p.heads);
+            for (int a = 0; a < kSmemQAtoms; ++a)
+                tma_load_2d(q_s + a * kQAtomBytes, &qmap, &ctl->q_full, a * 64, t * p.heads);
         }
-        if (!v_part) {  // warm L2 with the first tiles
+        if (warp == 0) {  // warm L2 with the first tiles
             for (int e = lane; e < kPrefetchTiles * kRows && e < ntiles * kRows; e += 32) {
                 const int32_t row = rows_s[e];
                 if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
             }
         }
         for (int i = 0; i < ntiles; ++i) {
-            if (!v_part) {
+            const int bsel = i & 1;
+            if (warp == 0) {
                 const int ahead = i + kPrefetchTiles;
                 if (ahead < ntiles) {
                     for (int e = lane; e < kRows; e += 32) {
@@ -218,85 +230,88 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                     }
                 }
             }
-            if (!mbar_wait(empty, ((uint32_t)i & 1u) ^ 1u, p.err)) break;
+            uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
+            uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+            const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
             const int c8 = lane & 7;
 #pragma unroll 1
-            for (int r0 = 0; r0 < kRows; r0 += 4) {
+            for (int r0 = row0; r0 < row0 + kRows / 2; r0 += 4) {
                 const int r = r0 + (lane >> 3);
                 const int32_t row = rows_s[i * kRows + r];
                 const uint16_t* src = p.kv_cache + (int64_t)row * kDim + c8 * 8;
-                const uint32_t row_base = smem_u32(kv_s) + r * 128 + ((c8 ^ (r & 7)) << 4);
+                const uint32_t row_base = base + r * 128 + ((c8 ^ (r & 7)) << 4);
 #pragma unroll
                 for (int a = 0; a < kAtoms; ++a) {
                     if (is_v_atom(a, dvh) != v_part) continue;
-                    const uint32_t dst = row_base + a * kAtomBytes;
+                    const uint32_t dst = row_base + part_slot(a, dvh) * kAtomBytes;
                     if (row >= 0)
                         cp_async_16(dst, src + a * 64);
                     else
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                        cp_async_zero16(dst, p.kv_cache);
                 }
             }
-            cp_async_commit();
-            cp_async_wait_group<0>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full);
+            // every lane signals once its own copies have landed; the warp moves on to the next tile at once
+            cp_async_mbar_arrive(full);
         }
-        cp_async_wait_group<0>();
-    } else if (warp == 1) {
-        // ---------------- MMA issuer: QK_K(i+1) -> PV(i) -> QK_V(i+1) ----------------
+        cp_async_wait_all();
+    }
+    else if (warp == 1) {
+        // ---------------- MMA issuer: S(i) = Q K(i)^T, then O += P(i-1) V(i-1) ----------------
         if (lane == 0) {
             bool ok = mbar_wait(&ctl->q_full, 0, p.err);
             ctl->q_waited = ok ? 1 : 0;
-            const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s);
-            // S(j) over the atoms of one part; the first MMA of the K part overwrites the accumulator
-            auto issue_qk_part = [&](int j, bool v_part) {
-                const uint32_t d = tmem + kSCol + (j & 1) * kRows;
-                bool first = !v_part;
-#pragma unroll
-                for (int a = 0; a < kAtoms; ++a) {
-                    if (is_v_atom(a, dvh) != v_part) continue;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc(q_base + a * (128 * 128) + kk * 32, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(kv_base + a * kAtomBytes + kk * 32, 16, 1024, kSwizzle128B);
-                        umma_f16_ss(d, ad, bd, kIdescQK, first ? 0u : 1u);
-                        first = false;
-                    }
-                }
-            };
-            auto qk_k = [&](int j) -> bool {  // needs the K part of tile j and a free S buffer
-                if (!mbar_wait(&ctl->k_full, (uint32_t)j & 1u, p.err)) return false;
-                if (!mbar_wait(&ctl->s_empty[j & 1], (((uint32_t)j >> 1) & 1u) ^ 1u, p.err)) return false;
+            ok = ok && mbar_wait(&ctl->qt_full, 0, p.err);
+            const uint32_t q_base = smem_u32(q_s), kb = smem_u32(kbuf), vb = smem_u32(vbuf);
+            auto pv = [&](int j) -> bool {
+                if (!mbar_wait(&ctl->p_full, (uint32_t)j & 1u, p.err)) return false;
                 tc_fence_after();
-                issue_qk_part(j, false);
-                umma_commit(&ctl->k_empty);
-                return true;
-            };
-            auto qk_v = [&](int j) -> bool {  // needs the V part of tile j
-                if (!mbar_wait(&ctl->v_full, (uint32_t)j & 1u, p.err)) return false;
-                tc_fence_after();
-                issue_qk_part(j, true);
-                umma_commit(&ctl->s_full[j & 1]);
-                return true;
-            };
-            if (ok && ntiles > 0) ok = qk_k(0) && qk_v(0);
-            for (int i = 0; ok && i < ntiles; ++i) {
-                if (i + 1 < ntiles && !qk_k(i + 1)) break;
-                if (!mbar_wait(&ctl->p_full[i & 1], ((uint32_t)i >> 1) & 1u, p.err)) break;
-                tc_fence_after();
+                const uint32_t vbase = vb + (j & 1) * kVBufBytes;
 #pragma unroll
                 for (int kk = 0; kk < kRows / 16; ++kk) {
                     // V part as an MN-major operand: 64-dim atoms kAtomBytes apart, 8-row groups 1024 B apart
-                    const uint64_t bd = smem_desc(kv_base + (dvh * 4) * kAtomBytes + kk * 2048, kAtomBytes, 1024,
-                                                  kSwizzle128B);
-                    umma_f16_ts(tmem, tmem + kPCol + (i & 1) * (kRows / 2) + kk * 8, bd, kIdescPV,
-                                (i > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t bd = smem_desc(vbase + kk * 2048, kAtomBytes, 1024, kSwizzle128B);
+                    umma_f16_ts(tmem, tmem + kPCol + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(&ctl->v_empty);
-                umma_commit(&ctl->p_empty[i & 1]);
-                if (i + 1 < ntiles && !qk_v(i + 1)) break;
+                umma_commit(&ctl->v_empty[j & 1]);
+                umma_commit(&ctl->p_empty);
+                return true;
+            };
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int bs = i & 1;
+                const uint32_t ph = ((uint32_t)i >> 1) & 1u;
+                if (!mbar_wait(&ctl->k_full[bs], ph, p.err) || !mbar_wait(&ctl->v_full[bs], ph, p.err) ||
+                    !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) {
+                    ok = false;
+                    break;
+                }
+                // the rows were written by cp.async (generic proxy); the MMAs read them through the async proxy
+                fence_proxy_async_smem();
+                tc_fence_after();
+                const uint32_t kbase = kb + bs * kKBufBytes, vbase = vb + bs * kVBufBytes;
+#pragma unroll
+                for (int a = 0; a < kAtoms; ++a) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t boff = part_slot(a, dvh) * kAtomBytes + kk * 32;
+                        const uint64_t bd = smem_desc((is_v_atom(a, dvh) ? vbase : kbase) + boff, 16, 1024, kSwizzle128B);
+                        const uint32_t acc = (a | kk) != 0 ? 1u : 0u;
+                        if (a < kSmemQAtoms) {
+                            const uint64_t ad = smem_desc(q_base + a * kQAtomBytes + kk * 32, 16, 1024, kSwizzle128B);
+                            umma_f16_ss(tmem + kSCol, ad, bd, kIdescQK, acc);
+                        } else {
+                            umma_f16_ts(tmem + kSCol, tmem + kQCol + (a - kSmemQAtoms) * 32 + kk * 8, bd, kIdescQK, acc);
+                        }
+                    }
+                }
+                umma_commit(&ctl->k_empty[bs]);
+                umma_commit(&ctl->s_full);
+                if (i > 0 && !pv(i - 1)) {
+                    ok = false;
+                    break;
+                }
             }
+            if (ok && ntiles > 0) pv(ntiles - 1);
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, p.err);
         }
@@ -304,24 +319,64 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
         // ---------------- softmax: one thread per head row ----------------
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t trow = tmem + ((quad * 32u) << 16);
+        {
+            // Q atoms 4-8 of this head row into TMEM (the A operand of those atoms' MMAs)
+            const int h = (int)quad * 32 + lane;
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.heads + h) * kDim + 64 * kSmemQAtoms);
+            constexpr int kGroups = (kAtoms - kSmemQAtoms) * 2;  // 16-column groups
+            static_assert(kGroups % 2 == 0, "two batches");
+#pragma unroll 1
+            for (int c0 = 0; c0 < kGroups; c0 += kGroups / 2) {
+                // one batch of independent 16-byte loads in flight, then the TMEM stores
+                uint32_t qv[kGroups / 2][16];
+#pragma unroll
+                for (int c = 0; c < kGroups / 2; ++c) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 v = h < p.heads ? __ldg(src + (c0 + c) * 4 + j) : make_uint4(0, 0, 0, 0);
+                        qv[c][4 * j] = v.x;
+                        qv[c][4 * j + 1] = v.y;
+                        qv[c][4 * j + 2] = v.z;
+                        qv[c][4 * j + 3] = v.w;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < kGroups / 2; ++c) tmem_st16_u32(trow + kQCol + (c0 + c) * 16, qv[c]);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->qt_full);
+        }
         for (int i = 0; i < ntiles; ++i) {
-            const int sb = i & 1;
             const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
             const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + 32 + lane] >= 0);
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full[sb], ((uint32_t)i >> 1) & 1u, p.err))) break;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full, (uint32_t)i & 1u, p.err))) break;
             tc_fence_after();
             float sv[kRows];
-#pragma unroll
-            for (int c = 0; c < kRows / 16; ++c) {
-                float a16[16];
-                tmem_ld16(trow + kSCol + sb * kRows + c * 16, a16);
+            {
+                // all four column groups in flight before one wait
+                float a0[16], a1[16], a2[16], a3[16];
+                tmem_ld16(trow + kSCol, a0);
+                tmem_ld16(trow + kSCol + 16, a1);
+                tmem_ld16(trow + kSCol + 32, a2);
+                tmem_ld16(trow + kSCol + 48, a3);
                 tmem_ld_wait();
+                tmem_regs_ready(a0);
+                tmem_regs_ready(a1);
+                tmem_regs_ready(a2);
+                tmem_regs_ready(a3);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) sv[c * 16 + j] = a16[j];
+                for (int j = 0; j < 16; ++j) {
+                    sv[j] = a0[j];
+                    sv[16 + j] = a1[j];
+                    sv[32 + j] = a2[j];
+                    sv[48 + j] = a3[j];
+                }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
+            if (lane == 0) mbar_arrive(&ctl->s_empty);
             float mt = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
@@ -332,24 +387,21 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
             const bool raise = mt > m_used + kRescaleLog2;
             const float m_new = raise ? mt : m_used;
             const float alpha = (raise && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
-            // the P buffer of this tile is free once P(i-2) V(i-2) has completed
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty[sb], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+            // P(i-1) V(i-1) has completed: the P columns are free and O is stable
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err))) break;
+            tc_fence_after();
             if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-                // rescaling O needs every earlier P V to have completed (i >= 1 here, since m_used was finite)
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty[sb ^ 1], ((uint32_t)(i - 1) >> 1) & 1u, p.err)))
-                    break;
-                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < kOCols / 16; ++c) {
                     float o[16];
                     tmem_ld16(trow + c * 16, o);
                     tmem_ld_wait();
+                    tmem_regs_ready(o);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) o[j] *= alpha;
                     tmem_st16(trow + c * 16, o);
                 }
             }
-            tc_fence_after();
             l_sum *= alpha;
             m_used = m_new;
             uint32_t packed[kRows / 2];
@@ -363,14 +415,14 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 rs += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
             }
             l_sum += rs;
-            tmem_st16_u32(trow + kPCol + sb * (kRows / 2), packed);
-            tmem_st16_u32(trow + kPCol + sb * (kRows / 2) + 16, packed + 16);
+            tmem_st16_u32(trow + kPCol, packed);
+            tmem_st16_u32(trow + kPCol + 16, packed + 16);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
+            if (lane == 0) mbar_arrive(&ctl->p_full);
         }
-        if (ntiles > 0) mbar_wait(&ctl->p_empty[(ntiles - 1) & 1], ((uint32_t)(ntiles - 1) >> 1) & 1u, p.err);
+        if (ntiles > 0) mbar_wait(&ctl->p_empty, ((uint32_t)(ntiles - 1)) & 1u, p.err);
         tc_fence_after();
     }
     tc_fence_before();
@@ -390,6 +442,7 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 float o[16];
                 tmem_ld16(trow + c * 16, o);
                 tmem_ld_wait();
+                tmem_regs_ready(o);
                 if (h < p.heads) {
                     uint32_t pk[8];
 #pragma unroll
@@ -407,7 +460,8 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
         // merge the P position splits of this value half through distributed shared memory
         if (softmax_thread) ctl->ml[h] = make_float2(m_used, l_sum);
         cluster_sync();
-        float* obuf = reinterpret_cast<float*>(q_s);  // Q is dead: every MMA has completed
+        // 128 rows x 1 KiB of fp32 partials over the Q and K-part buffers: every MMA and copy has completed
+        float* obuf = reinterpret_cast<float*>(q_s);
         if (softmax_thread) {
             float M = -INFINITY, Lsum = 0.f;
             float2 ml[8];
@@ -431,6 +485,7 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 float o[16];
                 tmem_ld16(trow + c * 16, o);
                 tmem_ld_wait();
+                tmem_regs_ready(o);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int qc = c * 4 + q4;  // 16-byte chunk index 0..63
@@ -485,6 +540,7 @@ cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
     while (P < 8 && P * 2 <= max_splits && (int64_t)p.total_q * 2 * (P * 2) <= L.num_sms) P *= 2;
     if ((p.top_k + P - 1) / P > kMaxEntries) return cudaErrorInvalidValue;
     p.splits = P;
+    static_assert(kQBytes + 2 * kKBufBytes >= 128 * 1024, "split merge buffer must fit in the Q and K-part buffers");
     if (kSfaSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSfaSmem);
     if (e != cudaSuccess) return e;
