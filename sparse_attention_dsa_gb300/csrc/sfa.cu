@@ -13,16 +13,21 @@
 //     atoms 0-3 stay in shared memory (SMEM A operand), atoms 4-8 live in tensor memory (TMEM A
 //     operand), which leaves shared memory for double-buffered row tiles;
 //   * at start every thread helps translate the split's selected positions (Top-K entry -> page table
-//     -> physical row) into a row list in smem, so no global lookup sits on the per-tile path;
+//     -> physical row) into a row list in smem, in two dependent rounds of independent loads (the
+//     entries together with a parallel search for the token's sequence, then the pages together with
+//     the sequence length), so no global lookup sits on the per-tile path;
 //   * the selected rows are processed 64 at a time (UMMA N = 64: below that a tcgen05.mma costs about
 //     as much as at N = 64).  Each tile is kept as the 256 value dims this CTA owns (the "V part") and
-//     the other 320 dims (the "K part"), each double-buffered.  Two pairs of gather warps refill them
+//     the other 320 dims (the "K part"), each double-buffered and refilled by its own four gather warps
 //     with cp.async pieces written straight into the 128B-swizzled operand layout (per-lane 16-byte
-//     copies issue faster here than TMA tile::gather4, which moves only 4 rows per copy) and prefetch
-//     rows a few tiles ahead into L2 (cp.async.bulk.prefetch);
-//   * the MMA issuer runs S(i) = Q K(i)^T, then O += P(i-1) V(i-1); the softmax of tile i (one thread per
-//     head row, online max raised only when it grows by more than 2^8 so O rarely needs rescaling)
-//     overlaps S(i+1) on the tensor pipe;
+//     copies issue faster here than TMA tile::gather4, which moves only 4 rows per copy).  The loads of
+//     a tile are issued about two tiles ahead of its use, which hides the HBM latency without an L2
+//     prefetch;
+//   * the MMA issuer runs S(i) = Q K(i)^T over the K part, then O += P(i-1) V(i-1), then the V-part
+//     atoms of S(i).  The V buffer of a tile is busy until its P V has run, so this order gives its
+//     refill a whole tile period; the K buffer is free as soon as the K-part MMAs of S(i) complete;
+//   * the softmax of tile i (one thread per head row, online max raised only when it grows by more
+//     than 2^8 so O rarely needs rescaling) overlaps the K-part MMAs of S(i+1);
 //   * O += P V (M=128, N=256, K=64; A = P from TMEM, B = the V part read as an MN-major operand)
 //     accumulates in TMEM.  The 512 value dims are split between the two CTAs of the pair (each owns 256
 //     columns of O) because a full 128 x 512 fp32 O would fill all of TMEM; both CTAs compute the same S.
@@ -39,7 +44,11 @@ namespace {
 
 constexpr int kDim = 576;  // latent + rope
 constexpr int kVDim = 512;
-constexpr int kThreadsSfa = 288;  // warps 0/7: K-part gather, 6/8: V-part gather, 1: MMA, 2-5: softmax
+// warp 0: Q load, 1: MMA, 2-5: softmax, then the K-part and the V-part gather warps
+constexpr int kKWarps = 4;
+constexpr int kVWarps = 4;
+constexpr int kFirstGatherWarp = 6;
+constexpr int kThreadsSfa = 32 * (kFirstGatherWarp + kKWarps + kVWarps);
 constexpr int kRows = 64;         // selected rows per tile
 constexpr int kAtoms = kDim / 64;  // 128-byte swizzle atoms per row
 constexpr int kSmemQAtoms = 4;     // Q atoms 0-3 in smem, 4-8 in TMEM
@@ -50,12 +59,14 @@ constexpr int kQBytes = kSmemQAtoms * kQAtomBytes;
 constexpr int kKBufBytes = kKAtoms * kAtomBytes;
 constexpr int kVBufBytes = 4 * kAtomBytes;
 constexpr int kMaxEntries = 2048;  // selected entries per CTA (per position split)
+constexpr int kEntPerThread = (kMaxEntries + kThreadsSfa - 1) / kThreadsSfa;
+constexpr int kMaxSplits = 8;
+constexpr int kMlRows = 128 + kMaxSplits;  // P * ceil(128 / P) rows at most
 constexpr int kOCols = 256;        // TMEM columns [0, 256): O (this CTA's value half)
 constexpr int kSCol = 256;         // [256, 320): S
 constexpr int kPCol = 320;         // [320, 352): P, 64 bf16 per row
 constexpr int kQCol = 352;         // [352, 512): Q atoms 4-8, 32 columns each
 constexpr int kTmemCols = 512;
-constexpr int kPrefetchTiles = 3;  // L2 prefetch distance, in tiles
 constexpr uint32_t kIdescQK = make_idesc(128, kRows, 1, 1, 0, 0);
 constexpr uint32_t kIdescPV = make_idesc(128, kOCols, 1, 1, 0, 1);
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only when it grows by more than this
@@ -70,7 +81,8 @@ struct SfaCtrl {
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t q_waited;
-    float2 ml[128];
+    int32_t tok_b, tok_cu0, tok_cu1;  // sequence of this CTA's query token and its query offsets
+    float2 ml[kMlRows];  // split merge: (max, sum) of the rows pushed to this CTA
 };
 
 constexpr size_t kSfaSmem =
@@ -93,6 +105,14 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// 2^x by the SFU approximation (relative error about 2^-22, far below the bf16 rounding of P);
+// ex2(-inf) = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -100,10 +120,6 @@ __device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* v)
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
         "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Atom a (64 dims) of a row belongs to the V part of the CTA that owns value half dvh.
@@ -130,59 +146,78 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     const int ps = (blockIdx.x >> 1) % P;
     const int t = blockIdx.x / (2 * P);
     if (t >= p.total_q) return;  // uniform over the cluster
-    int b = 0;
-    {
-        int lo = 0, hi = p.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.cu_q_lens + mid) <= t) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-    }
-    const int cu0 = __ldg(p.cu_q_lens + b), cu1 = __ldg(p.cu_q_lens + b + 1);
-    const int n_b = cu1 - cu0;
-    const int L = __ldg(p.seq_lens + b);
-    if (t < cu0 || t >= cu1 || n_b > L || L > p.max_pages * 64) {
-        if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
-        return;  // uniform over the cluster (same token)
-    }
-    const int64_t pos = (int64_t)L - n_b + (t - cu0);
     const int per = ((p.top_k + P - 1) / P + kRows - 1) / kRows * kRows;
     const int e0 = ps * per;
     const int n_ent = max(0, min(p.top_k, e0 + per) - e0);
     const int ntiles = (n_ent + kRows - 1) / kRows;
 
-    // ---- translate this split's entries into physical rows (all threads, independent loads) ----
+    // ---- translate this split's entries into physical rows: two dependent rounds of independent loads ----
+    // round 1: the split's Top-K entries, and a parallel search for the sequence that holds token t
+    int32_t ent[kEntPerThread];
     {
         const int32_t* sel = p.topk + (int64_t)t * p.top_k + e0;
-        const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
-        for (int e = tid; e < ntiles * kRows; e += kThreadsSfa) {
-            int32_t row = -1;
-            if (e < n_ent) {
-                const int32_t s = __ldg(sel + e);
-                if (s >= 0) {
-                    if ((int64_t)s > pos) {
-                        if (dvh == 0) raise_error(p.err, DSA_DEVERR_INDEX);
-                    } else {
-                        const int32_t pg = __ldg(pt_row + (s >> 6));
-                        if (pg < 0 || pg >= p.num_pages) {
-                            if (dvh == 0) raise_error(p.err, DSA_DEVERR_PAGE);
-                        } else {
-                            row = pg * 64 + (s & 63);
-                        }
-                    }
-                }
-            }
-            rows_s[e] = row;
+#pragma unroll
+        for (int k = 0; k < kEntPerThread; ++k) {
+            const int e = tid + k * kThreadsSfa;
+            ent[k] = e < n_ent ? __ldg(sel + e) : -1;
         }
+    }
+    if (tid == 0) ctl->tok_b = -1;
+    __syncthreads();
+    for (int j = tid; j < p.batch; j += kThreadsSfa) {
+        const int c0 = __ldg(p.cu_q_lens + j), c1 = __ldg(p.cu_q_lens + j + 1);
+        if (c0 <= t && t < c1) {  // one sequence when the offsets are non-decreasing
+            ctl->tok_b = j;
+            ctl->tok_cu0 = c0;
+            ctl->tok_cu1 = c1;
+        }
+    }
+    __syncthreads();
+    const int b = ctl->tok_b;
+    if (b < 0) {
+        if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
+        return;  // uniform over the cluster (same token)
+    }
+    // round 2: the sequence length and the page of every entry (speculative: checked against pos below)
+    const int cu0 = ctl->tok_cu0, cu1 = ctl->tok_cu1;
+    const int n_b = cu1 - cu0;
+    const int L = __ldg(p.seq_lens + b);
+    int32_t pg[kEntPerThread];
+    {
+        const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
+#pragma unroll
+        for (int k = 0; k < kEntPerThread; ++k)
+            pg[k] = (ent[k] >= 0 && (ent[k] >> 6) < p.max_pages) ? __ldg(pt_row + (ent[k] >> 6)) : -1;
+    }
+    if (n_b > L || L > p.max_pages * 64) {
+        if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
+        return;  // uniform over the cluster (same token)
+    }
+    const int64_t pos = (int64_t)L - n_b + (t - cu0);
+#pragma unroll
+    for (int k = 0; k < kEntPerThread; ++k) {
+        const int e = tid + k * kThreadsSfa;
+        if (e >= ntiles * kRows) continue;
+        int32_t row = -1;
+        const int32_t s_pos = ent[k];
+        if (s_pos >= 0) {
+            if ((int64_t)s_pos > pos) {
+                if (dvh == 0) raise_error(p.err, DSA_DEVERR_INDEX);
+            } else if (pg[k] < 0 || pg[k] >= p.num_pages) {
+                if (dvh == 0) raise_error(p.err, DSA_DEVERR_PAGE);
+            } else {
+                row = pg[k] * 64 + (s_pos & 63);
+            }
+        }
+        rows_s[e] = row;
     }
     if (tid == 0) {
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->qt_full, 4);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl->k_full[i], 64);  // one cp.async-tracked arrival per gather lane
+            mbar_init(&ctl->k_full[i], 32 * kKWarps);  // one cp.async-tracked arrival per gather lane
             mbar_init(&ctl->k_empty[i], 1);
-            mbar_init(&ctl->v_full[i], 64);
+            mbar_init(&ctl->v_full[i], 32 * kVWarps);
             mbar_init(&ctl->v_empty[i], 1);
         }
         mbar_init(&ctl->s_full, 1);
@@ -203,40 +238,29 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     const uint32_t tmem = ctl->tmem_base;
 
     float m_used = -INFINITY, l_sum = 0.f;  // softmax threads: running max (log2 units) and sum
-    if (warp == 0 || warp >= 6) {
-        // ---------------- gather: warps 0/7 fill the K part, warps 6/8 the V part, 32 rows each ----------------
-        const bool v_part = warp == 6 || warp == 8;
-        const int row0 = (warp == 7 || warp == 8) ? kRows / 2 : 0;
-        if (warp == 0 && lane == 0) {
+    if (warp == 0) {
+        // ---------------- Q atoms 0-3 (TMA) ----------------
+        if (lane == 0) {
             prefetch_tensormap(&qmap);
             mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
             for (int a = 0; a < kSmemQAtoms; ++a)
                 tma_load_2d(q_s + a * kQAtomBytes, &qmap, &ctl->q_full, a * 64, t * p.heads);
         }
-        if (warp == 0) {  // warm L2 with the first tiles
-            for (int e = lane; e < kPrefetchTiles * kRows && e < ntiles * kRows; e += 32) {
-                const int32_t row = rows_s[e];
-                if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
-            }
-        }
+    } else if (warp >= kFirstGatherWarp) {
+        // ---------------- gather: kKWarps warps fill the K part, kVWarps warps the V part ----------------
+        const int gw = warp - kFirstGatherWarp;
+        const bool v_part = gw >= kKWarps;
+        const int pw = v_part ? gw - kKWarps : gw;  // warp index within its part
+        const int nw = v_part ? kVWarps : kKWarps;
+        const int c8 = lane & 7;
         for (int i = 0; i < ntiles; ++i) {
             const int bsel = i & 1;
-            if (warp == 0) {
-                const int ahead = i + kPrefetchTiles;
-                if (ahead < ntiles) {
-                    for (int e = lane; e < kRows; e += 32) {
-                        const int32_t row = rows_s[ahead * kRows + e];
-                        if (row >= 0) prefetch_l2(p.kv_cache + (int64_t)row * kDim, kDim * 2);
-                    }
-                }
-            }
             uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
             uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
             const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
-            const int c8 = lane & 7;
 #pragma unroll 1
-            for (int r0 = row0; r0 < row0 + kRows / 2; r0 += 4) {
+            for (int r0 = 4 * pw; r0 < kRows; r0 += 4 * nw) {
                 const int r = r0 + (lane >> 3);
                 const int32_t row = rows_s[i * kRows + r];
                 const uint16_t* src = p.kv_cache + (int64_t)row * kDim + c8 * 8;
@@ -277,25 +301,17 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 umma_commit(&ctl->p_empty);
                 return true;
             };
-            for (int i = 0; ok && i < ntiles; ++i) {
-                const int bs = i & 1;
-                const uint32_t ph = ((uint32_t)i >> 1) & 1u;
-                if (!mbar_wait(&ctl->k_full[bs], ph, p.err) || !mbar_wait(&ctl->v_full[bs], ph, p.err) ||
-                    !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) {
-                    ok = false;
-                    break;
-                }
-                // the rows were written by cp.async (generic proxy); the MMAs read them through the async proxy
-                fence_proxy_async_smem();
-                tc_fence_after();
-                const uint32_t kbase = kb + bs * kKBufBytes, vbase = vb + bs * kVBufBytes;
+            // S(i) over the atoms of one part (the K part first: it starts the accumulation)
+            auto qk = [&](int i, bool v_atoms) {
+                const uint32_t kbase = kb + (i & 1) * kKBufBytes, vbase = vb + (i & 1) * kVBufBytes;
 #pragma unroll
                 for (int a = 0; a < kAtoms; ++a) {
+                    if (is_v_atom(a, dvh) != v_atoms) continue;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t boff = part_slot(a, dvh) * kAtomBytes + kk * 32;
-                        const uint64_t bd = smem_desc((is_v_atom(a, dvh) ? vbase : kbase) + boff, 16, 1024, kSwizzle128B);
-                        const uint32_t acc = (a | kk) != 0 ? 1u : 0u;
+                        const uint64_t bd = smem_desc((v_atoms ? vbase : kbase) + boff, 16, 1024, kSwizzle128B);
+                        const uint32_t acc = (v_atoms || part_slot(a, dvh) != 0 || kk != 0) ? 1u : 0u;
                         if (a < kSmemQAtoms) {
                             const uint64_t ad = smem_desc(q_base + a * kQAtomBytes + kk * 32, 16, 1024, kSwizzle128B);
                             umma_f16_ss(tmem + kSCol, ad, bd, kIdescQK, acc);
@@ -304,12 +320,32 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                         }
                     }
                 }
-                umma_commit(&ctl->k_empty[bs]);
-                umma_commit(&ctl->s_full);
+            };
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const uint32_t ph = ((uint32_t)i >> 1) & 1u;
+                // K part of S(i): needs its rows and the softmax to have read S(i-1)
+                if (!mbar_wait(&ctl->k_full[i & 1], ph, p.err) ||
+                    !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) {
+                    ok = false;
+                    break;
+                }
+                // the rows were written by cp.async (generic proxy); the MMAs read them through the async proxy
+                fence_proxy_async_smem();
+                tc_fence_after();
+                qk(i, false);
+                umma_commit(&ctl->k_empty[i & 1]);
                 if (i > 0 && !pv(i - 1)) {
                     ok = false;
                     break;
                 }
+                if (!mbar_wait(&ctl->v_full[i & 1], ph, p.err)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_smem();
+                tc_fence_after();
+                qk(i, true);
+                umma_commit(&ctl->s_full);
             }
             if (ok && ntiles > 0) pv(ntiles - 1);
             umma_commit(&ctl->mma_done);
@@ -377,16 +413,36 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->s_empty);
-            float mt = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
                 const uint32_t m = j < 32 ? vm0 : vm1;
                 sv[j] = ((m >> (j & 31)) & 1u) ? sv[j] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sv[j]);
             }
+            // row max as a tree (short dependency chains)
+            float mx[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) mx[k] = fmaxf(fmaxf(sv[k], sv[k + 16]), fmaxf(sv[k + 32], sv[k + 48]));
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
+            const float mt = mx[0];
             const bool raise = mt > m_used + kRescaleLog2;
             const float m_new = raise ? mt : m_used;
             const float alpha = (raise && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
+            // P before the wait for P(i-1) V(i-1): only the P store and an O rescale need it done.  With no
+            // row seen yet every score is -inf, and exp2(-inf - 0) = 0.
+            const float mu = m_new == -INFINITY ? 0.f : m_new;
+            uint32_t packed[kRows / 2];
+            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < kRows; j += 2) {
+                const uint32_t pk = f2_to_bf2(ex2_approx(sv[j] - mu), ex2_approx(sv[j + 1] - mu));
+                packed[j / 2] = pk;
+                // the row sum takes the bf16-rounded values that P V uses
+                ps[(j / 2) & 7] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+            }
+            const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             // P(i-1) V(i-1) has completed: the P columns are free and O is stable
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err))) break;
             tc_fence_after();
@@ -402,19 +458,8 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                     tmem_st16(trow + c * 16, o);
                 }
             }
-            l_sum *= alpha;
+            l_sum = l_sum * alpha + rs;
             m_used = m_new;
-            uint32_t packed[kRows / 2];
-            float rs = 0.f;
-#pragma unroll
-            for (int j = 0; j < kRows; j += 2) {
-                const float x0 = m_used == -INFINITY ? 0.f : exp2f(sv[j] - m_used);
-                const float x1 = m_used == -INFINITY ? 0.f : exp2f(sv[j + 1] - m_used);
-                const uint32_t pk = f2_to_bf2(x0, x1);
-                packed[j / 2] = pk;
-                rs += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
-            }
-            l_sum += rs;
             tmem_st16_u32(trow + kPCol, packed);
             tmem_st16_u32(trow + kPCol + 16, packed + 16);
             tmem_st_wait();
@@ -457,71 +502,98 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 p.lse[(int64_t)t * p.heads + h] = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
     } else {
-        // merge the P position splits of this value half through distributed shared memory
-        if (softmax_thread) ctl->ml[h] = make_float2(m_used, l_sum);
-        cluster_sync();
-        // 128 rows x 1 KiB of fp32 partials over the Q and K-part buffers: every MMA and copy has completed
+        // Merge the P position splits of this value half.  Split j owns head rows [j*slice, (j+1)*slice).
+        // Every CTA pushes each of its O rows, with that row's (max, sum), into the owner's shared memory
+        // (fire-and-forget DSMEM stores); after one cluster barrier each owner combines its rows locally.
+        // Receive buffer (over the Q and K-part buffers): row j*slice + r, 1 KiB of fp32 with its 16-byte
+        // chunks XOR-swizzled by the row, holds split j's partial O of the owner's head ps*slice + r.
+        const int slice = (128 + P - 1) / P;
         float* obuf = reinterpret_cast<float*>(q_s);
+        cluster_sync();  // every CTA of the cluster is past its main loop: the Q and K buffers are free
         if (softmax_thread) {
-            float M = -INFINITY, Lsum = 0.f;
-            float2 ml[8];
-            const uint32_t ml_addr = smem_u32(&ctl->ml[h]);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j < P) {
-                    const uint32_t a = mapa_shared(ml_addr, (uint32_t)(dvh + 2 * j));
-                    float2 v;
-                    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-                    ml[j] = v;
-                    M = fmaxf(M, v.x);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < P && ml[j].y > 0.f) Lsum += ml[j].y * exp2f(ml[j].x - M);
-            const float f = (l_sum > 0.f && Lsum > 0.f) ? exp2f(m_used - M) / Lsum : 0.f;
+            const int owner = h / slice, r = h % slice;
+            const int R = ps * slice + r;  // row in the owner's receive buffer
+            const uint32_t local_row = smem_u32(obuf) + R * 1024;
+            const bool remote = owner != ps;
+            const uint32_t dst = (uint32_t)(dvh + 2 * owner);
+            const uint32_t row_addr = remote ? mapa_shared(local_row, dst) : local_row;
+            const uint32_t ml_local = smem_u32(&ctl->ml[R]);
+            if (remote)
+                asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(mapa_shared(ml_local, dst)), "f"(m_used),
+                             "f"(l_sum)
+                             : "memory");
+            else
+                ctl->ml[R] = make_float2(m_used, l_sum);
 #pragma unroll 1
-            for (int c = 0; c < kOCols / 16; ++c) {
-                float o[16];
-                tmem_ld16(trow + c * 16, o);
-                tmem_ld_wait();
-                tmem_regs_ready(o);
+            for (int c = 0; c < kOCols / 16; c += 4) {
+                float o[4][16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int qc = c * 4 + q4;  // 16-byte chunk index 0..63
-                    const uint32_t dst = smem_u32(obuf) + h * 1024 + ((qc ^ (h & 63)) << 4);
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(o[4 * q4] * f),
-                                 "f"(o[4 * q4 + 1] * f), "f"(o[4 * q4 + 2] * f), "f"(o[4 * q4 + 3] * f)
-                                 : "memory");
+                for (int u = 0; u < 4; ++u) tmem_ld16(trow + (c + u) * 16, o[u]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 4; ++u) tmem_regs_ready(o[u]);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float* v = &o[q >> 2][4 * (q & 3)];
+                    const int qc = c * 4 + q;  // 16-byte chunk 0..63
+                    const uint32_t a = row_addr + ((qc ^ (R & 7)) << 4);
+                    if (remote)
+                        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[0]), "f"(v[1]),
+                                     "f"(v[2]), "f"(v[3])
+                                     : "memory");
+                    else
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+                                     "f"(v[3])
+                                     : "memory");
                 }
             }
-            const int slice = 128 / P;
-            if (dvh == 0 && h / slice == ps && h < p.heads && p.lse)
-                p.lse[(int64_t)t * p.heads + h] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         }
-        cluster_sync();
-        if (softmax_thread) {
-            const int slice = 128 / P;
-            const int h0 = ps * slice;
-            const int stid = tid - 64;  // 0..127
-            for (int idx = stid; idx < slice * 64; idx += 128) {
-                const int hh = h0 + idx / 64;
-                const int qc = idx % 64;
-                if (hh >= p.heads) continue;
-                const uint32_t local = smem_u32(obuf) + hh * 1024 + ((qc ^ (hh & 63)) << 4);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int j = 0; j < P; ++j) {
-                    const float4 v = ld_dsmem_f4(mapa_shared(local, (uint32_t)(dvh + 2 * j)));
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-                const uint2 pk = make_uint2(f2_to_bf2(acc.x, acc.y), f2_to_bf2(acc.z, acc.w));
-                *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + hh) * kVDim + dvh * kOCols + qc * 4) = pk;
+        cluster_sync();  // all pushes have landed
+        // per row of the slice: the weight of every split, exp2(m_j - M) / sum_j l_j exp2(m_j - M), and lse
+        float* wgt = reinterpret_cast<float*>(rows_s);  // [kMaxSplits][slice]; the row list is no longer needed
+        if (tid < slice) {
+            const int r = tid;
+            float M = -INFINITY;
+            for (int j = 0; j < P; ++j) {
+                const float2 v = ctl->ml[j * slice + r];
+                if (v.y > 0.f) M = fmaxf(M, v.x);
             }
+            float Lsum = 0.f;
+            for (int j = 0; j < P; ++j) {
+                const float2 v = ctl->ml[j * slice + r];
+                if (v.y > 0.f) Lsum += v.y * exp2f(v.x - M);
+            }
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            for (int j = 0; j < P; ++j) {
+                const float2 v = ctl->ml[j * slice + r];
+                // a split with no selected row adds nothing (and its O is never read)
+                wgt[j * slice + r] = v.y > 0.f ? exp2f(v.x - M) * inv : 0.f;
+            }
+            const int hh = ps * slice + r;
+            if (dvh == 0 && hh < p.heads && p.lse)
+                p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         }
-        cluster_sync();  // peers may still be reading this CTA's buffers
+        __syncthreads();
+        // combine: every thread takes (row, 16-byte chunk) items of this CTA's slice
+        const int rows_here = min(slice, p.heads - ps * slice);
+        for (int idx = tid; idx < rows_here * 64; idx += kThreadsSfa) {
+            const int r = idx >> 6, qc = idx & 63;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < P; ++j) {
+                const float wj = wgt[j * slice + r];
+                if (wj == 0.f) continue;
+                const int R = j * slice + r;
+                const float4 o = *reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(obuf) + R * 1024 +
+                                                                  ((qc ^ (R & 7)) << 4));
+                acc.x += o.x * wj;
+                acc.y += o.y * wj;
+                acc.z += o.z * wj;
+                acc.w += o.w * wj;
+            }
+            const uint2 pk = make_uint2(f2_to_bf2(acc.x, acc.y), f2_to_bf2(acc.z, acc.w));
+            *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + ps * slice + r) * kVDim + dvh * kOCols + qc * 4) = pk;
+        }
+        // no DSMEM access follows the second barrier, so a CTA may exit as soon as its own rows are written
     }
     tc_fence_before();
     __syncthreads();
@@ -531,21 +603,53 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
 
 }  // namespace
 
+// Clusters of `size` CTAs of this kernel that can be resident at once (cached per device and size).
+static int max_active_clusters(int size) {
+    static int cache[64][2 * kMaxSplits + 1];  // 0 = not queried yet
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int& c = cache[dev][size];
+    if (c == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)size;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)size);
+        cfg.blockDim = dim3(kThreadsSfa);
+        cfg.dynamicSmemBytes = kSfaSmem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, sfa_kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        c = n > 0 ? n : -1;
+    }
+    return c;
+}
+
 cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
     SfaParams p = L.params;
-    // position splits: enough CTAs to cover the SMs, and at most kMaxEntries entries per split
-    int P = 1;
-    while (P < 8 && (p.top_k + P - 1) / P > kMaxEntries) P *= 2;
-    const int max_splits = (p.top_k + kRows - 1) / kRows;
-    while (P < 8 && P * 2 <= max_splits && (int64_t)p.total_q * 2 * (P * 2) <= L.num_sms) P *= 2;
-    if ((p.top_k + P - 1) / P > kMaxEntries) return cudaErrorInvalidValue;
-    p.splits = P;
-    static_assert(kQBytes + 2 * kKBufBytes >= 128 * 1024, "split merge buffer must fit in the Q and K-part buffers");
+    static_assert(kQBytes + 2 * kKBufBytes >= kMlRows * 1024, "split merge buffer must fit in the Q and K-part buffers");
     if (kSfaSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSfaSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+    // Position splits P (a cluster of 2P CTAs per query token): the fewest that keep a split within
+    // kMaxEntries entries, grown while the CTAs still fit on the SMs, then shrunk until every cluster
+    // of the grid can be resident at once (a second wave of clusters would double the time).
+    int P = 1;
+    while (P < kMaxSplits && (p.top_k + P - 1) / P > kMaxEntries) ++P;
+    if ((p.top_k + P - 1) / P > kMaxEntries) return cudaErrorInvalidValue;
+    const int min_p = P;
+    const int max_splits = (p.top_k + kRows - 1) / kRows;
+    while (P < kMaxSplits && P + 1 <= max_splits && (int64_t)p.total_q * 2 * (P + 1) <= L.num_sms) ++P;
+    while (P > min_p && P > 1 && p.total_q > max_active_clusters(2 * P)) --P;
+    p.splits = P;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
