@@ -36,7 +36,6 @@ constexpr int kThreads = 256;
 constexpr int kTileM = 128;  // positions per tile (two pages)
 constexpr int kPage = 64;
 constexpr int kMaxCluster = 16;
-constexpr int kPrefetchTiles = 4;  // tiles prefetched into L2 beyond the smem ring
 
 template <int HI, int DI, int QB, bool FP8>
 struct IdxCfg {
@@ -65,8 +64,6 @@ struct SelectSmem {
     uint32_t ecnt[kMaxCluster];
     uint32_t scan_e[kThreads / 32];
     uint32_t scan_s[kThreads / 32];
-    uint32_t bstar;
-    uint32_t remaining;
     uint32_t take_me;
     uint32_t off_me;
 };
@@ -90,9 +87,9 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // Cluster-wide Top-K of one query.  keys: this CTA's n local keys (position range_start + i);
-// hist0: this CTA's histogram of the keys' top byte, built while scoring; allh: C x 256 scratch for the
-// gathered per-CTA histograms.  visible = p + 1 positions exist in total.  All CTAs of the cluster call
-// this with identical (K, visible), so the cluster barriers inside match up.
+// hist0: this CTA's histogram of the keys' top byte, built while scoring; allh: 2 x C x 256 scratch for
+// the gathered per-CTA histograms.  visible = p + 1 positions exist in total.  All CTAs of the cluster
+// call this with identical (K, visible), so the cluster barriers inside match up.
 __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, int n, int K,
                                int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
                                SelectSmem& S) {
@@ -113,13 +110,11 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         if (pass > 0) {  // the top-byte histogram (pass 0) was built while scoring
             S.hist[buf][tid] = 0;
             __syncthreads();
+            // plain shared atomics: the keys spread over many bins here, where a warp-level match would
+            // cost one round per distinct bin
             for (int i = tid; i < n; i += kThreads) {
                 const uint32_t key = keys[i];
-                if (((key ^ prefix) & hmask) == 0) {
-                    const uint32_t bin = (key >> shift) & 255u;
-                    const uint32_t peers = __match_any_sync(__activemask(), bin);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[buf][bin], (uint32_t)__popc(peers));
-                }
+                if (((key ^ prefix) & hmask) == 0) atomicAdd(&S.hist[buf][(key >> shift) & 255u], 1u);
             }
             __syncthreads();
         }
@@ -137,31 +132,38 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
             S.totals[tid] = tot;
         }
         __syncthreads();
-        if (warp == 0) {
+        // every warp finds the bin that holds the remaining-th largest key itself (no broadcast barrier)
+        uint32_t bstar = 0, rem_in = 0;
+        {
             uint32_t v[8], lsum = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 v[j] = S.totals[lane * 8 + j];
                 lsum += v[j];
             }
-            uint32_t incl = lsum;
+            uint32_t incl = lsum;  // sum over lanes >= this one (bins at or above lane*8)
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, off);
                 if (lane + off < 32) incl += t;
             }
             uint32_t above = incl - lsum;
+            uint32_t found = 0, fb = 0, fr = 0;
 #pragma unroll
             for (int j = 7; j >= 0; --j) {
                 if (above < remaining && remaining <= above + v[j]) {
-                    S.bstar = (uint32_t)(lane * 8 + j);
-                    S.remaining = remaining - above;
+                    found = 1;
+                    fb = (uint32_t)(lane * 8 + j);
+                    fr = remaining - above;
                 }
                 above += v[j];
             }
+            const uint32_t who = __ballot_sync(0xFFFFFFFFu, found != 0);
+            const int src_lane = who ? __ffs(who) - 1 : 0;
+            bstar = __shfl_sync(0xFFFFFFFFu, fb, src_lane);
+            rem_in = __shfl_sync(0xFFFFFFFFu, fr, src_lane);
         }
-        __syncthreads();
-        const uint32_t bstar = S.bstar;
+        // keys above the boundary bin, per source CTA (warp r handles CTA r, r + 8, ...)
         for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
             uint32_t s = 0;
             for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? ah[r * 256 + i] : 0u;
@@ -170,11 +172,11 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
             if (lane == 0) S.gt[r] += s;
         }
         if (pass == 3 && tid < (int)C) S.ecnt[tid] = ah[tid * 256 + bstar];
-        remaining = S.remaining;
+        remaining = rem_in;
         prefix |= bstar << shift;
-        __syncthreads();
     }
     const uint32_t T = prefix;
+    __syncthreads();  // the per-CTA counts (gt, ecnt) are complete
     if (tid == 0) {
         uint32_t ties_before = 0, running = 0;
         for (uint32_t r = 0; r < C; ++r) {
@@ -329,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- scoring pipeline -----------------------------------------------------------------------------
     if (ntiles > 0) {
+        // The producer and MMA warps run their loops with all 32 lanes (every lane waits on the barriers,
+        // one lane issues), so no lane of these warps sits at the block barrier while the loop runs.
         if (warp == 0) {
             if (lane == 0) {
                 prefetch_tensormap(&kmap);
@@ -337,24 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int a = 0; a < Cfg::kAtoms; ++a)
                     tma_load_2d(q_tile + a * Cfg::kN * 128, &qmap, &ctl->qbar, a * (128 / Cfg::kElem), t0 * HI);
-                // L2 prefetch keeps kPrefetchTiles more tiles in flight than the smem ring holds
-                auto prefetch_tile = [&](int j) {
-                    if (j >= ntiles) return;
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int32_t pg = pages_s[2 * j + h2];
-                        if (pg < 0) continue;
-#pragma unroll
-                        for (int a = 0; a < Cfg::kAtoms; ++a) tma_prefetch_3d(&kmap, a * (128 / Cfg::kElem), 0, pg);
-                    }
-                };
-                for (int j = S; j < S + kPrefetchTiles; ++j) prefetch_tile(j);
-                int issued = 0;
-                for (int i = 0; i < ntiles; ++i) {
-                    const int s = i % S;
-                    const uint32_t ph = (uint32_t)(i / S) & 1u;
-                    prefetch_tile(i + S + kPrefetchTiles);
-                    if (!mbar_wait(&ctl->empty[s], ph ^ 1u, p.err)) break;
+            }
+            int issued = 0;
+            int s = 0;  // ring slot and its phase, advanced without a division by the runtime depth
+            uint32_t ph = 0;
+            for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->empty[s], ph ^ 1u, p.err))) break;
+                if (lane == 0) {
                     const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
                     const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * (kPage * Cfg::kRowBytes);
                     if (bytes == 0) {
@@ -372,26 +365,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             a * (128 / Cfg::kElem), 0, pg1);
                         }
                     }
-                    issued = i + 1;
                 }
-                ctl->issued = issued;
+                __syncwarp();
+                issued = i + 1;
             }
+            if (lane == 0) ctl->issued = issued;
         } else if (warp == 1) {
-            if (lane == 0) {
-                const uint32_t tmem = ctl->tmem_base;
-                const uint32_t q_base = smem_u32(q_tile);
-                int consumed = 0;
-                bool ok = mbar_wait(&ctl->qbar, 0, p.err);
-                ctl->qwaited = ok ? 1 : 0;
-                for (int i = 0; ok && i < ntiles; ++i) {
-                    const int s = i % S;
-                    const uint32_t ph = (uint32_t)(i / S) & 1u;
-                    const int ab = i % Cfg::kAccBufs;
-                    const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
-                    if (!mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err)) break;
-                    if (!mbar_wait(&ctl->full[s], ph, p.err)) break;
-                    consumed = i + 1;
-                    tc_fence_after();
+            const uint32_t tmem = ctl->tmem_base;
+            const uint32_t q_base = smem_u32(q_tile);
+            int consumed = 0;
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err));
+            if (lane == 0) ctl->qwaited = ok ? 1 : 0;
+            int s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                const int ab = i % Cfg::kAccBufs;
+                const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->full[s], ph, p.err))) break;
+                consumed = i + 1;
+                tc_fence_after();
+                if (lane == 0) {
                     const uint32_t a_base = smem_u32(a_tiles + (size_t)s * Cfg::kStageBytes);
 #pragma unroll
                     for (int k = 0; k < Cfg::kKSteps; ++k) {
@@ -407,8 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(&ctl->empty[s]);
                     umma_commit(&ctl->tfull[ab]);
                 }
-                ctl->consumed = consumed;
+                __syncwarp();
             }
+            if (lane == 0) ctl->consumed = consumed;
         } else if (warp >= 2 && warp < 6) {
             const uint32_t quad = (uint32_t)(warp & 3);  // TMEM lanes this warp may access
             const int row = (int)quad * 32 + lane;       // position within the tile
@@ -429,6 +424,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float acc[QB];
 #pragma unroll
                 for (int q = 0; q < QB; ++q) acc[q] = 0.f;
+                if constexpr (HI % 32 == 0) {
+                    // One query's heads, 32 columns per TMEM wait, in a rolled loop: the code stays small
+                    // (it shares the instruction cache with the MMA warp), eight independent partial sums
+                    // keep the FMA chains short, and the weights come four at a time.
+#pragma unroll
+                    for (int q = 0; q < QB; ++q) {
+                        float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                        for (int c0 = q * HI; c0 < (q + 1) * HI; c0 += 32) {
+                            float v0[16], v1[16];
+                            tmem_ld16(tmem + ab * Cfg::kN + c0, v0);
+                            tmem_ld16(tmem + ab * Cfg::kN + c0 + 16, v1);
+                            tmem_ld_wait();
+                            tmem_regs_ready(v0);
+                            tmem_regs_ready(v1);
+                            const float4* w4 = reinterpret_cast<const float4*>(w_s + c0);
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                const float4 wv = w4[j4];
+                                const float* v = j4 < 4 ? v0 + 4 * j4 : v1 + 4 * (j4 - 4);
+                                part[(2 * j4) & 7] = fmaf(wv.x, fmaxf(v[0], 0.f), part[(2 * j4) & 7]);
+                                part[(2 * j4 + 1) & 7] = fmaf(wv.y, fmaxf(v[1], 0.f), part[(2 * j4 + 1) & 7]);
+                                part[(2 * j4) & 7] = fmaf(wv.z, fmaxf(v[2], 0.f), part[(2 * j4) & 7]);
+                                part[(2 * j4 + 1) & 7] = fmaf(wv.w, fmaxf(v[3], 0.f), part[(2 * j4 + 1) & 7]);
+                            }
+                        }
+                        acc[q] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                    }
+                } else
 #pragma unroll
                 for (int c0 = 0; c0 < Cfg::kNReal; c0 += 32) {
                     float v0[16], v1[16];
@@ -484,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_select(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, n_keys, p.top_k, visible,
                        p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel);
     }
-    cluster_sync();  // peers may still read this CTA's histograms
+    // No cluster barrier here: every remote access is a histogram push, and the pushes of a pass complete
+    // before that pass's barrier, so after the last pass no CTA touches another's shared memory.
 }
 
 template <int HI, int DI, int QB, bool FP8>
