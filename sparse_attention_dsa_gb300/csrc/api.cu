@@ -241,9 +241,11 @@ dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_
     return DSA_OK;
 }
 
+// after_indexer: the previous launch on this stream is this library's indexer, made in the same call on the
+// same inputs, so the attention kernel may start before it ends (it waits on the device for the Top-K).
 dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
                      const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out, float* lse,
-                     void* workspace, void* stream) {
+                     void* workspace, void* stream, bool after_indexer = false) {
     dsa_status_t st = check_common(d);
     if (st) return st;
     if (d->attn_heads < 1) return fail(DSA_ERR_INVALID_ARG, "attn_heads must be >= 1 (got %d)", d->attn_heads);
@@ -289,6 +291,7 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
     p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
     L.smem_limit = dev.smem_optin;
     L.num_sms = dev.num_sms;
+    L.after_indexer = after_indexer;
     {
         EncodeTiledFn enc = encode_fn();
         if (!enc) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -354,7 +357,9 @@ dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const f
     dsa_status_t st = run_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx,
                                   workspace, stream);
     if (st) return st;
-    return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream);
+    // the indexer was launched on this stream just now whenever there is a query token
+    return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream,
+                   dims->total_q > 0);
 }
 
 dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* code) {

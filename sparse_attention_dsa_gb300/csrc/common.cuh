@@ -134,6 +134,13 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 
 // ----------------------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched right behind another may start early; it must wait
+// before reading what that kernel writes.  Both are no-ops without such a launch.
+// ----------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------------------------------
 // Thread-block clusters and distributed shared memory
 // ----------------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -252,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + 2 * cluster_nctarank() * 256);
     CtrlSmem* ctl = reinterpret_cast<CtrlSmem*>((reinterpret_cast<uintptr_t>(sel + 1) + 15) & ~uintptr_t(15));
 
+    // the attention kernel queued behind this one may be scheduled now: it waits on the device before it
+    // reads the Top-K this kernel writes
+    allow_dependent_launch();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t C = cluster_nctarank();
     const uint32_t rank = cluster_ctarank();

@@ -70,6 +70,7 @@ struct SfaParams {
     int32_t v_dim;
     float scale_log2;  // softmax_scale * log2(e)
     int32_t splits;    // position splits per query (filled in by the launcher)
+    int32_t early_setup;  // launched right behind this library's indexer: only topk comes from it
 };
 
 struct SfaLaunch {
@@ -77,6 +78,7 @@ struct SfaLaunch {
     SfaParams params;
     int smem_limit;
     int num_sms;
+    bool after_indexer;  // the previous kernel in the stream is this library's indexer (programmatic launch)
 };
 
 cudaError_t launch_sfa(const SfaLaunch& launch, cudaStream_t stream);

@@ -151,17 +151,22 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     const int n_ent = max(0, min(p.top_k, e0 + per) - e0);
     const int ntiles = (n_ent + kRows - 1) / kRows;
 
-    // ---- translate this split's entries into physical rows: two dependent rounds of independent loads ----
-    // round 1: the split's Top-K entries, and a parallel search for the sequence that holds token t
+    // ---- set-up.  Launched right behind this library's indexer (early_setup), everything up to the wait
+    // below overlaps the indexer's tail: only the Top-K entries come from it.  Otherwise any input may come
+    // from the previous kernel in the stream, so the kernel waits first.
+    if (tid == 0) prefetch_tensormap(&qmap);
+    if (!p.early_setup) grid_dependency_wait();
     int32_t ent[kEntPerThread];
-    {
+    auto load_entries = [&]() {
         const int32_t* sel = p.topk + (int64_t)t * p.top_k + e0;
 #pragma unroll
         for (int k = 0; k < kEntPerThread; ++k) {
             const int e = tid + k * kThreadsSfa;
             ent[k] = e < n_ent ? __ldg(sel + e) : -1;
         }
-    }
+    };
+    if (!p.early_setup) load_entries();  // overlaps the sequence search
+    // the sequence that holds token t: a parallel search over the query offsets
     if (tid == 0) ctl->tok_b = -1;
     __syncthreads();
     for (int j = tid; j < p.batch; j += kThreadsSfa) {
@@ -178,39 +183,14 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
         if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
         return;  // uniform over the cluster (same token)
     }
-    // round 2: the sequence length and the page of every entry (speculative: checked against pos below)
     const int cu0 = ctl->tok_cu0, cu1 = ctl->tok_cu1;
     const int n_b = cu1 - cu0;
     const int L = __ldg(p.seq_lens + b);
-    int32_t pg[kEntPerThread];
-    {
-        const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
-#pragma unroll
-        for (int k = 0; k < kEntPerThread; ++k)
-            pg[k] = (ent[k] >= 0 && (ent[k] >> 6) < p.max_pages) ? __ldg(pt_row + (ent[k] >> 6)) : -1;
-    }
     if (n_b > L || L > p.max_pages * 64) {
         if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
         return;  // uniform over the cluster (same token)
     }
     const int64_t pos = (int64_t)L - n_b + (t - cu0);
-#pragma unroll
-    for (int k = 0; k < kEntPerThread; ++k) {
-        const int e = tid + k * kThreadsSfa;
-        if (e >= ntiles * kRows) continue;
-        int32_t row = -1;
-        const int32_t s_pos = ent[k];
-        if (s_pos >= 0) {
-            if ((int64_t)s_pos > pos) {
-                if (dvh == 0) raise_error(p.err, DSA_DEVERR_INDEX);
-            } else if (pg[k] < 0 || pg[k] >= p.num_pages) {
-                if (dvh == 0) raise_error(p.err, DSA_DEVERR_PAGE);
-            } else {
-                row = pg[k] * 64 + (s_pos & 63);
-            }
-        }
-        rows_s[e] = row;
-    }
     if (tid == 0) {
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->qt_full, 4);
@@ -236,17 +216,75 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    if (tid == 0) {
+        // Q atoms 0-3 into shared memory (TMA)
+        mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+        for (int a = 0; a < kSmemQAtoms; ++a) tma_load_2d(q_s + a * kQAtomBytes, &qmap, &ctl->q_full, a * 64, t * p.heads);
+    }
+    if (warp >= 2 && warp < 6) {
+        // Q atoms 4-8 of this head row into TMEM (the A operand of those atoms' MMAs)
+        const uint32_t quad = (uint32_t)(warp & 3);
+        const uint32_t trow = tmem + ((quad * 32u) << 16);
+        const int h = (int)quad * 32 + lane;
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.heads + h) * kDim + 64 * kSmemQAtoms);
+        constexpr int kGroups = (kAtoms - kSmemQAtoms) * 2;  // 16-column groups
+        static_assert(kGroups % 2 == 0, "two batches");
+#pragma unroll 1
+        for (int c0 = 0; c0 < kGroups; c0 += kGroups / 2) {
+            // one batch of independent 16-byte loads in flight, then the TMEM stores
+            uint32_t qv[kGroups / 2][16];
+#pragma unroll
+            for (int c = 0; c < kGroups / 2; ++c) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 v = h < p.heads ? __ldg(src + (c0 + c) * 4 + j) : make_uint4(0, 0, 0, 0);
+                    qv[c][4 * j] = v.x;
+                    qv[c][4 * j + 1] = v.y;
+                    qv[c][4 * j + 2] = v.z;
+                    qv[c][4 * j + 3] = v.w;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < kGroups / 2; ++c) tmem_st16_u32(trow + kQCol + (c0 + c) * 16, qv[c]);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->qt_full);
+    }
+    // ---- this split's entries -> physical rows (the Top-K entries, then their pages) ----
+    if (p.early_setup) {
+        grid_dependency_wait();
+        load_entries();
+    }
+    int32_t pg[kEntPerThread];
+    {
+        const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
+#pragma unroll
+        for (int k = 0; k < kEntPerThread; ++k)
+            pg[k] = (ent[k] >= 0 && (ent[k] >> 6) < p.max_pages) ? __ldg(pt_row + (ent[k] >> 6)) : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < kEntPerThread; ++k) {
+        const int e = tid + k * kThreadsSfa;
+        if (e >= ntiles * kRows) continue;
+        int32_t row = -1;
+        const int32_t s_pos = ent[k];
+        if (s_pos >= 0) {
+            if ((int64_t)s_pos > pos) {
+                if (dvh == 0) raise_error(p.err, DSA_DEVERR_INDEX);
+            } else if (pg[k] < 0 || pg[k] >= p.num_pages) {
+                if (dvh == 0) raise_error(p.err, DSA_DEVERR_PAGE);
+            } else {
+                row = pg[k] * 64 + (s_pos & 63);
+            }
+        }
+        rows_s[e] = row;
+    }
+    __syncthreads();
 
     float m_used = -INFINITY, l_sum = 0.f;  // softmax threads: running max (log2 units) and sum
-    if (warp == 0) {
-        // ---------------- Q atoms 0-3 (TMA) ----------------
-        if (lane == 0) {
-            prefetch_tensormap(&qmap);
-            mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
-            for (int a = 0; a < kSmemQAtoms; ++a)
-                tma_load_2d(q_s + a * kQAtomBytes, &qmap, &ctl->q_full, a * 64, t * p.heads);
-        }
-    } else if (warp >= kFirstGatherWarp) {
+    if (warp >= kFirstGatherWarp) {
         // ---------------- gather: kKWarps warps fill the K part, kVWarps warps the V part ----------------
         const int gw = warp - kFirstGatherWarp;
         const bool v_part = gw >= kKWarps;
@@ -351,39 +389,10 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, p.err);
         }
-    } else {
+    } else if (warp >= 2) {
         // ---------------- softmax: one thread per head row ----------------
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t trow = tmem + ((quad * 32u) << 16);
-        {
-            // Q atoms 4-8 of this head row into TMEM (the A operand of those atoms' MMAs)
-            const int h = (int)quad * 32 + lane;
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.heads + h) * kDim + 64 * kSmemQAtoms);
-            constexpr int kGroups = (kAtoms - kSmemQAtoms) * 2;  // 16-column groups
-            static_assert(kGroups % 2 == 0, "two batches");
-#pragma unroll 1
-            for (int c0 = 0; c0 < kGroups; c0 += kGroups / 2) {
-                // one batch of independent 16-byte loads in flight, then the TMEM stores
-                uint32_t qv[kGroups / 2][16];
-#pragma unroll
-                for (int c = 0; c < kGroups / 2; ++c) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 v = h < p.heads ? __ldg(src + (c0 + c) * 4 + j) : make_uint4(0, 0, 0, 0);
-                        qv[c][4 * j] = v.x;
-                        qv[c][4 * j + 1] = v.y;
-                        qv[c][4 * j + 2] = v.z;
-                        qv[c][4 * j + 3] = v.w;
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < kGroups / 2; ++c) tmem_st16_u32(trow + kQCol + (c0 + c) * 16, qv[c]);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->qt_full);
-        }
         for (int i = 0; i < ntiles; ++i) {
             const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
             const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + 32 + lane] >= 0);
@@ -548,6 +557,7 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 }
             }
         }
+        __syncthreads();  // the threads with nothing to push wait here rather than in the cluster barrier
         cluster_sync();  // all pushes have landed
         // per row of the slice: the weight of every split, exp2(m_j - M) / sum_j l_j exp2(m_j - M), and lse
         float* wgt = reinterpret_cast<float*>(rows_s);  // [kMaxSplits][slice]; the row list is no longer needed
@@ -574,24 +584,44 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         }
         __syncthreads();
-        // combine: every thread takes (row, 16-byte chunk) items of this CTA's slice
+        // combine: every thread takes (row, 16-byte chunk) items of this CTA's slice, three at a time so
+        // their shared-memory loads overlap
         const int rows_here = min(slice, p.heads - ps * slice);
-        for (int idx = tid; idx < rows_here * 64; idx += kThreadsSfa) {
-            const int r = idx >> 6, qc = idx & 63;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int n_items = rows_here * 64;
+        const uint32_t obuf_base = smem_u32(obuf), wgt_base = smem_u32(wgt);
+        for (int idx0 = tid; idx0 < n_items; idx0 += 3 * kThreadsSfa) {
+            float4 acc[3];
+#pragma unroll
+            for (int u = 0; u < 3; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < P; ++j) {
-                const float wj = wgt[j * slice + r];
-                if (wj == 0.f) continue;
-                const int R = j * slice + r;
-                const float4 o = *reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(obuf) + R * 1024 +
-                                                                  ((qc ^ (R & 7)) << 4));
-                acc.x += o.x * wj;
-                acc.y += o.y * wj;
-                acc.z += o.z * wj;
-                acc.w += o.w * wj;
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int idx = idx0 + u * kThreadsSfa;
+                    const int r = (idx < n_items ? idx : 0) >> 6, qc = idx & 63;
+                    const int R = j * slice + r;
+                    float wj;
+                    float4 o;
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(wj) : "r"(wgt_base + (uint32_t)(j * slice + r) * 4u));
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(o.x), "=f"(o.y), "=f"(o.z), "=f"(o.w)
+                                 : "r"(obuf_base + (uint32_t)R * 1024u + ((uint32_t)(qc ^ (R & 7)) << 4)));
+                    // a split with no selected row has weight 0 and an O that is never written: select, not scale
+                    const bool use = wj != 0.f;
+                    acc[u].x += use ? o.x * wj : 0.f;
+                    acc[u].y += use ? o.y * wj : 0.f;
+                    acc[u].z += use ? o.z * wj : 0.f;
+                    acc[u].w += use ? o.w * wj : 0.f;
+                }
             }
-            const uint2 pk = make_uint2(f2_to_bf2(acc.x, acc.y), f2_to_bf2(acc.z, acc.w));
-            *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + ps * slice + r) * kVDim + dvh * kOCols + qc * 4) = pk;
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int idx = idx0 + u * kThreadsSfa;
+                if (idx >= n_items) continue;
+                const int r = idx >> 6, qc = idx & 63;
+                const uint2 pk = make_uint2(f2_to_bf2(acc[u].x, acc[u].y), f2_to_bf2(acc[u].z, acc[u].w));
+                *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + ps * slice + r) * kVDim + dvh * kOCols + qc * 4) =
+                    pk;
+            }
         }
         // no DSMEM access follows the second barrier, so a CTA may exit as soon as its own rows are written
     }
@@ -650,18 +680,22 @@ cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
     while (P < kMaxSplits && P + 1 <= max_splits && (int64_t)p.total_q * 2 * (P + 1) <= L.num_sms) ++P;
     while (P > min_p && P > 1 && p.total_q > max_active_clusters(2 * P)) --P;
     p.splits = P;
+    p.early_setup = L.after_indexer ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)(P == 1 ? 1 : 2 * P);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // right behind the indexer: start early, wait on the device before reading the Top-K
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)(p.total_q * 2 * P));
     cfg.blockDim = dim3(kThreadsSfa);
     cfg.dynamicSmemBytes = kSfaSmem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = L.after_indexer ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, sfa_kernel, L.qmap, p);
 }
 
