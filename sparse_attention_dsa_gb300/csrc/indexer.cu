@@ -10,9 +10,11 @@
 //
 // Work decomposition: one thread-block cluster of C CTAs per (sequence, block of up to QB query tokens).
 // CTA r of the cluster scores positions [r*chunk, (r+1)*chunk) of that sequence and keeps the scores as
-// order-preserving uint32 keys in its own shared memory.  A cluster-wide radix select (4 passes of 8
-// bits; histograms exchanged through distributed shared memory) then finds the K-th key, and every CTA
-// writes its selected positions in ascending order at an offset derived from the per-CTA counts.
+// order-preserving uint32 keys in its own shared memory.  A cluster-wide radix select (8-bit digits,
+// most significant first; histograms and, for the last two bytes, the surviving candidate keys
+// exchanged through distributed shared memory, usually in two rounds) then finds the K-th key, and
+// every CTA writes its selected positions in ascending order at an offset derived from the per-CTA
+// counts.
 //
 // Scoring pipeline inside a CTA (warp-specialised):
 //   warp 0  : TMA producer.  Each 128-position tile is two 64-token pages of the indexer K cache,
@@ -54,16 +56,28 @@ struct IdxCfg {
                                      : (kAccBufs * kN) <= 128 ? 128 : (kAccBufs * kN) <= 256 ? 256 : 512;
     static constexpr uint32_t kIdesc = make_idesc(128, kN, FP8 ? 0u : 1u, FP8 ? 0u : 1u, 0u, 0u);
     static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
+    // the select's fallback exchange space (2 x C x 256 words) lives in the stage ring (at least 2 stages)
+    static_assert(2 * kStageBytes >= 2 * kMaxCluster * 256 * 4, "stage ring too small for the select");
     static_assert(kN <= 256, "UMMA N limit");
+    static_assert(QB <= 4, "per-query select state is sized for four queries");
 };
 
+constexpr int kCandCap = 256;  // second-round candidates one CTA may send (a power of two)
+
+// Words of the per-CTA page list: one per 64-position page, rounded up to whole 16-byte units.
+__host__ __device__ constexpr int page_words(int chunk) { return ((chunk / kPage) + 3) & ~3; }
+
 struct SelectSmem {
-    uint32_t hist[2][256];
-    uint32_t totals[256];
-    uint32_t gt[kMaxCluster];
-    uint32_t ecnt[kMaxCluster];
+    alignas(16) uint32_t hist[2][256];
+    alignas(16) uint32_t totals[256];
+    uint32_t res[8];                 // results broadcast from the warp that finds a boundary bin
+    uint32_t gt[kMaxCluster];        // keys above the boundary found so far, per CTA of the cluster
+    uint32_t ecnt[kMaxCluster];      // keys equal to the K-th key, per CTA
+    uint32_t guess_in[kMaxCluster];  // round A: every CTA's guess of the top byte (pushed by that CTA)
+    uint32_t ncand_in[kMaxCluster];  // round B: every CTA's candidate count (pushed by that CTA)
     uint32_t scan_e[kThreads / 32];
     uint32_t scan_s[kThreads / 32];
+    uint32_t ncand;
     uint32_t take_me;
     uint32_t off_me;
 };
@@ -86,12 +100,107 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// Cluster-wide Top-K of one query.  keys: this CTA's n local keys (position range_start + i);
-// hist0: this CTA's histogram of the keys' top byte, built while scoring; allh: 2 x C x 256 scratch for
-// the gathered per-CTA histograms.  visible = p + 1 positions exist in total.  All CTAs of the cluster
-// call this with identical (K, visible), so the cluster barriers inside match up.
-__device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, int n, int K,
-                               int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
+// The bin of `totals` (256 bins, ascending key order, 16-byte aligned) that holds the remaining-th largest
+// key, and that key's rank inside the bin.  Called by one warp; every lane gets the result.
+__device__ __forceinline__ void boundary_bin(const uint32_t* totals, uint32_t remaining, uint32_t& bstar,
+                                             uint32_t& rem) {
+    const int lane = threadIdx.x & 31;
+    uint32_t v[8], lsum = 0;
+    {
+        const uint4 a = reinterpret_cast<const uint4*>(totals)[2 * lane];
+        const uint4 b = reinterpret_cast<const uint4*>(totals)[2 * lane + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) lsum += v[j];
+    uint32_t incl = lsum;  // keys in the bins at or above lane*8
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, off);
+        if (lane + off < 32) incl += t;
+    }
+    uint32_t above = incl - lsum;
+    uint32_t found = 0, fb = 0, fr = 0;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+        if (above < remaining && remaining <= above + v[j]) {
+            found = 1;
+            fb = (uint32_t)(lane * 8 + j);
+            fr = remaining - above;
+        }
+        above += v[j];
+    }
+    const uint32_t who = __ballot_sync(0xFFFFFFFFu, found != 0);
+    const int src = who ? __ffs(who) - 1 : 0;
+    bstar = __shfl_sync(0xFFFFFFFFu, fb, src);
+    rem = __shfl_sync(0xFFFFFFFFu, fr, src);
+}
+
+// S.gt[r] += the keys of CTA r in bins above bstar (its histogram: ah[r * stride + bin]).
+__device__ __forceinline__ void add_above(const uint32_t* ah, int stride, uint32_t bstar, uint32_t C, SelectSmem& S) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
+        uint32_t s = 0;
+        for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? ah[r * stride + i] : 0u;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        if (lane == 0) S.gt[r] += s;
+    }
+}
+
+// One radix pass with a cluster-wide histogram: this CTA's keys that match `prefix` above bit shift+8 are
+// counted by their byte at `shift`, every CTA's histogram is pushed into slot [rank] of `buf` ([C][256]) in
+// every CTA of the cluster, and all CTAs find the same boundary bin.
+__device__ void exchange_pass(const uint32_t* keys, int n, uint32_t prefix, int shift, uint32_t* buf, uint32_t rank,
+                              uint32_t C, uint32_t& remaining, uint32_t& bstar, SelectSmem& S) {
+    const int tid = threadIdx.x;
+    const uint32_t hmask = 0xFFFFFFFFu << (shift + 8);
+    S.hist[0][tid] = 0;
+    __syncthreads();
+    // plain shared atomics: a warp-level match would cost one round per distinct bin
+    for (int i = tid; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if (((key ^ prefix) & hmask) == 0) atomicAdd(&S.hist[0][(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    const uint32_t slot = smem_u32(buf + rank * 256 + tid);
+    for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), S.hist[0][tid]);
+    cluster_sync();
+    uint32_t tot = 0;
+    for (uint32_t r = 0; r < C; ++r) tot += buf[r * 256 + tid];
+    S.totals[tid] = tot;
+    __syncthreads();
+    if (tid < 32) {
+        uint32_t b, rem;
+        boundary_bin(S.totals, remaining, b, rem);
+        if (tid == 0) {
+            S.res[0] = b;
+            S.res[1] = rem;
+        }
+    }
+    __syncthreads();
+    bstar = S.res[0];
+    remaining = S.res[1];
+    add_above(buf, 256, bstar, C, S);
+    __syncthreads();  // S.totals, S.hist and S.res are reused next
+}
+
+// Cluster-wide Top-K of one query: the K largest of the cluster's keys, as positions in ascending order.
+//   keys: this CTA's n keys (position range_start + i); hist0: their top-byte histogram, built while
+//   scoring; allh: C x 768 words of exchange space that nothing but this function touches; sbuf:
+//   2 x C x 256 words of further exchange space that peers may write once every CTA of the cluster has
+//   finished scoring.
+// The K-th key is found radix-fashion, most significant byte first, with two cluster rounds in the usual
+// case: round A exchanges the top-byte histograms together with a second-byte histogram of the bin each
+// CTA guesses will hold the K-th key (the bin where its own count from the top reaches its share of K);
+// when every guess is the agreed top byte, the second byte is settled in the same round.  Round B sends
+// every key that still matches
+// the 16-bit prefix (usually a few dozen per CTA) to every CTA, which finds the exact K-th key among them.
+// A wrong guess or too many candidates falls back to a full exchanged pass per byte.  All CTAs of the
+// cluster call this with identical (K, visible), so the cluster barriers inside match up.
+__device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, uint32_t* sbuf, int n,
+                               int K, int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
                                SelectSmem& S) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (visible <= K) {  // every visible position is kept: 0..p in order, then -1
@@ -100,82 +209,188 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         for (int s = lo + tid; s < hi; s += kThreads) out_row[s] = (int64_t)s < visible ? s : -1;
         return;
     }
-    uint32_t prefix = 0, remaining = (uint32_t)K;
+    uint32_t remaining = (uint32_t)K, prefix = 0, bstar = 0;
     if (tid < kMaxCluster) S.gt[tid] = 0;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-        const int buf = pass & 1;
-        uint32_t* ah = allh + buf * C * 256;  // this pass's gathered histograms, [C][256]
-        if (pass > 0) {  // the top-byte histogram (pass 0) was built while scoring
-            S.hist[buf][tid] = 0;
-            __syncthreads();
-            // plain shared atomics: the keys spread over many bins here, where a warp-level match would
-            // cost one round per distinct bin
-            for (int i = tid; i < n; i += kThreads) {
-                const uint32_t key = keys[i];
-                if (((key ^ prefix) & hmask) == 0) atomicAdd(&S.hist[buf][(key >> shift) & 255u], 1u);
+    uint32_t* ahA = allh;             // round A: [C][512] = top-byte | guessed second-byte histograms
+    uint32_t* cand = allh + C * 512;  // round B: [C][kCandCap] candidate keys
+    static_assert(kCandCap <= 256, "round-B candidates share the 768-word slot");
+
+    // ---- round A: the top-byte histogram, and the second-byte histogram of the guessed bin ----
+    if (tid < 32) {
+        uint32_t g, gr;
+        boundary_bin(hist0, (uint32_t)((K + (int)C - 1) / (int)C), g, gr);
+        if (tid == 0) S.res[7] = g;
+    }
+    S.hist[1][tid] = 0;
+    __syncthreads();
+    const uint32_t guess = S.res[7];
+    for (int i0 = 4 * tid; i0 < n; i0 += 4 * kThreads * 8) {
+        uint4 k8[8];  // eight 16-byte loads in flight (n is a multiple of 128)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 4 * kThreads;
+            k8[u] = i < n ? *reinterpret_cast<const uint4*>(keys + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t kv[4] = {k8[u].x, k8[u].y, k8[u].z, k8[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (i0 + u * 4 * kThreads < n && (kv[e] >> 24) == guess) atomicAdd(&S.hist[1][(kv[e] >> 16) & 255u], 1u);
+        }
+    }
+    __syncthreads();
+    {
+        const uint32_t slot = smem_u32(ahA + rank * 512 + tid);
+        const uint32_t h0 = hist0[tid], h1 = S.hist[1][tid];
+        for (uint32_t r = 0; r < C; ++r) {
+            const uint32_t a = mapa_shared(slot, r);
+            st_dsmem_u32(a, h0);
+            st_dsmem_u32(a + 256 * 4, h1);
+        }
+        if (tid < (int)C) st_dsmem_u32(mapa_shared(smem_u32(&S.guess_in[rank]), (uint32_t)tid), guess);
+    }
+    cluster_sync();  // also: every CTA of the cluster has finished scoring, so sbuf may now be written
+    {
+        uint32_t t0 = 0, t1 = 0;
+        for (uint32_t r = 0; r < C; ++r) {
+            t0 += ahA[r * 512 + tid];
+            t1 += ahA[r * 512 + 256 + tid];
+        }
+        S.totals[tid] = t0;
+        S.hist[0][tid] = t1;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        uint32_t b0, r0, b1 = 0, r1 = 0;
+        boundary_bin(S.totals, remaining, b0, r0);
+        // the guessed second-byte histograms count the right keys when every CTA guessed this bin
+        const bool agree = __all_sync(0xFFFFFFFFu, lane >= (int)C || S.guess_in[lane] == b0);
+        if (agree) boundary_bin(S.hist[0], r0, b1, r1);
+        if (tid == 0) {
+            S.res[0] = b0;
+            S.res[1] = r0;
+            S.res[2] = agree ? 1u : 0u;
+            S.res[3] = b1;
+            S.res[4] = r1;
+        }
+    }
+    __syncthreads();
+    bstar = S.res[0];
+    remaining = S.res[1];
+    const bool spec = S.res[2] != 0;
+    add_above(ahA, 512, bstar, C, S);
+    prefix = bstar << 24;
+    if (spec) {
+        bstar = S.res[3];
+        remaining = S.res[4];
+        add_above(ahA + 256, 512, bstar, C, S);
+        __syncthreads();  // S.res is reused
+    } else {
+        __syncthreads();
+        exchange_pass(keys, n, prefix, 16, sbuf, rank, C, remaining, bstar, S);
+    }
+    prefix |= bstar << 16;
+
+    // ---- round B: the keys that still match the 16-bit prefix, sent to every CTA ----
+    if (tid == 0) S.ncand = 0;
+    __syncthreads();
+    for (int i0 = 4 * tid; i0 < n; i0 += 4 * kThreads * 8) {
+        uint4 k8[8];  // eight 16-byte loads in flight (n is a multiple of 128)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 4 * kThreads;
+            k8[u] = i < n ? *reinterpret_cast<const uint4*>(keys + i) : make_uint4(0, 0, 0, 0);
+        }
+        // matches are rare: mark them in a mask here, send them from a small rolled loop below (one copy of
+        // the sending code instead of 32)
+        uint32_t mask = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t kv[4] = {k8[u].x, k8[u].y, k8[u].z, k8[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (i0 + u * 4 * kThreads < n && ((kv[e] ^ prefix) & 0xFFFF0000u) == 0) mask |= 1u << (4 * u + e);
+        }
+#pragma unroll 1
+        while (mask != 0) {
+            const int bit = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const uint32_t key = keys[i0 + (bit >> 2) * 4 * kThreads + (bit & 3)];
+            const uint32_t j = atomicAdd(&S.ncand, 1u);
+            if (j < (uint32_t)kCandCap) {
+                const uint32_t slot = smem_u32(cand + rank * kCandCap + j);
+                for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), key);
             }
-            __syncthreads();
         }
-        {
-            // push this CTA's bin count into slot [rank] of every CTA's buffer (posted remote stores);
-            // the cluster barrier below makes them visible
-            const uint32_t v = pass == 0 ? hist0[tid] : S.hist[buf][tid];
-            const uint32_t slot = smem_u32(ah + rank * 256 + tid);
-            for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), v);
-        }
-        cluster_sync();
-        {
-            uint32_t tot = 0;
-            for (uint32_t r = 0; r < C; ++r) tot += ah[r * 256 + tid];
-            S.totals[tid] = tot;
+    }
+    __syncthreads();
+    if (tid < (int)C) st_dsmem_u32(mapa_shared(smem_u32(&S.ncand_in[rank]), (uint32_t)tid), S.ncand);
+    cluster_sync();
+    const bool fits = __syncthreads_and(tid >= (int)C || S.ncand_in[tid] <= (uint32_t)kCandCap) != 0;
+    uint32_t T;
+    if (fits) {
+        // every CTA holds the same candidate set: find the remaining-th largest among them locally
+        S.hist[0][tid] = 0;
+        S.hist[1][tid] = 0;
+        __syncthreads();
+        for (int idx = tid; idx < (int)C * kCandCap; idx += kThreads) {
+            const uint32_t r = (uint32_t)idx / kCandCap, j = (uint32_t)idx % kCandCap;
+            if (j < S.ncand_in[r]) atomicAdd(&S.hist[0][(cand[idx] >> 8) & 255u], 1u);
         }
         __syncthreads();
-        // every warp finds the bin that holds the remaining-th largest key itself (no broadcast barrier)
-        uint32_t bstar = 0, rem_in = 0;
-        {
-            uint32_t v[8], lsum = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v[j] = S.totals[lane * 8 + j];
-                lsum += v[j];
+        if (tid < 32) {
+            uint32_t b2, r2;
+            boundary_bin(S.hist[0], remaining, b2, r2);
+            if (tid == 0) {
+                S.res[0] = b2;
+                S.res[1] = r2;
             }
-            uint32_t incl = lsum;  // sum over lanes >= this one (bins at or above lane*8)
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, off);
-                if (lane + off < 32) incl += t;
-            }
-            uint32_t above = incl - lsum;
-            uint32_t found = 0, fb = 0, fr = 0;
-#pragma unroll
-            for (int j = 7; j >= 0; --j) {
-                if (above < remaining && remaining <= above + v[j]) {
-                    found = 1;
-                    fb = (uint32_t)(lane * 8 + j);
-                    fr = remaining - above;
-                }
-                above += v[j];
-            }
-            const uint32_t who = __ballot_sync(0xFFFFFFFFu, found != 0);
-            const int src_lane = who ? __ffs(who) - 1 : 0;
-            bstar = __shfl_sync(0xFFFFFFFFu, fb, src_lane);
-            rem_in = __shfl_sync(0xFFFFFFFFu, fr, src_lane);
         }
-        // keys above the boundary bin, per source CTA (warp r handles CTA r, r + 8, ...)
+        __syncthreads();
+        const uint32_t b2 = S.res[0];
+        remaining = S.res[1];
+        for (int idx = tid; idx < (int)C * kCandCap; idx += kThreads) {
+            const uint32_t r = (uint32_t)idx / kCandCap, j = (uint32_t)idx % kCandCap;
+            if (j < S.ncand_in[r] && ((cand[idx] >> 8) & 255u) == b2) atomicAdd(&S.hist[1][cand[idx] & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            uint32_t b3, r3;
+            boundary_bin(S.hist[1], remaining, b3, r3);
+            if (tid == 0) {
+                S.res[2] = b3;
+                S.res[3] = r3;
+            }
+        }
+        __syncthreads();
+        remaining = S.res[3];
+        T = prefix | (b2 << 8) | S.res[2];
+        // per CTA: its candidates above the K-th key and equal to it
         for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
-            uint32_t s = 0;
-            for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? ah[r * 256 + i] : 0u;
+            uint32_t cg = 0, ce = 0;
+            for (uint32_t j = (uint32_t)lane; j < S.ncand_in[r]; j += 32) {
+                const uint32_t key = cand[r * kCandCap + j];
+                cg += key > T ? 1u : 0u;
+                ce += key == T ? 1u : 0u;
+            }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-            if (lane == 0) S.gt[r] += s;
+            for (int off = 16; off > 0; off >>= 1) {
+                cg += __shfl_xor_sync(0xFFFFFFFFu, cg, off);
+                ce += __shfl_xor_sync(0xFFFFFFFFu, ce, off);
+            }
+            if (lane == 0) {
+                S.gt[r] += cg;
+                S.ecnt[r] = ce;
+            }
         }
-        if (pass == 3 && tid < (int)C) S.ecnt[tid] = ah[tid * 256 + bstar];
-        remaining = rem_in;
-        prefix |= bstar << shift;
+    } else {
+        exchange_pass(keys, n, prefix, 8, sbuf + C * 256, rank, C, remaining, bstar, S);
+        prefix |= bstar << 8;
+        exchange_pass(keys, n, prefix, 0, sbuf, rank, C, remaining, bstar, S);
+        T = prefix | bstar;
+        if (tid < (int)C) S.ecnt[tid] = sbuf[tid * 256 + bstar];
     }
-    const uint32_t T = prefix;
     __syncthreads();  // the per-CTA counts (gt, ecnt) are complete
     if (tid == 0) {
         uint32_t ties_before = 0, running = 0;
@@ -192,18 +407,27 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     }
     __syncthreads();
     const uint32_t take_me = S.take_me, off_me = S.off_me;
-    // Ordered compaction.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of the local keys:
-    // one pass counts its keys above T and its ties, a block barrier turns the counts into per-warp
-    // offsets, a second pass writes the selected positions in order.
+    // Ordered compaction.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of the local keys: one
+    // pass counts its keys above T and its ties, a block barrier turns the counts into per-warp offsets,
+    // a second pass writes the selected positions in order.  Both passes load four groups of 32 keys
+    // before using them, so the shared-memory latency is not paid once per group.
     const int nw = kThreads / 32;
-    const int seg = ((n + nw - 1) / nw + 31) / 32 * 32;
+    const int seg = ((n + nw - 1) / nw + 127) / 128 * 128;
     const int lo = warp * seg, hi = min(n, lo + seg);
     uint32_t cnt_gt = 0, cnt_tie = 0;
-    for (int base = lo; base < hi; base += 32) {
-        const int i = base + lane;
-        const uint32_t key = i < hi ? keys[i] : 0u;
-        cnt_gt += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, key > T));
-        cnt_tie += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, key == T && i < hi));
+    for (int base = lo; base < hi; base += 128) {
+        uint32_t k4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * 32 + lane;
+            k4[u] = i < hi ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool in = base + u * 32 + lane < hi;
+            cnt_gt += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, in && k4[u] > T));
+            cnt_tie += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, in && k4[u] == T));
+        }
     }
     if (lane == 0) {
         S.scan_e[warp] = cnt_tie;
@@ -219,17 +443,26 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     }
     if (cnt_gt == 0 && (cnt_tie == 0 || tie_base >= take_me)) return;  // nothing selected in this segment
     uint32_t run_tie = tie_base, run_sel = 0;
-    for (int base = lo; base < hi; base += 32) {
-        const int i = base + lane;
-        const uint32_t key = i < hi ? keys[i] : 0u;
-        const bool e = key == T && i < hi, g = key > T;
-        const uint32_t be = __ballot_sync(0xFFFFFFFFu, e);
-        const uint32_t tie_rank = run_tie + (uint32_t)__popc(be & lanemask_lt());
-        const bool sel = g || (e && tie_rank < take_me);
-        const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
-        if (sel) out_row[out_base + run_sel + (uint32_t)__popc(bs & lanemask_lt())] = range_start + i;
-        run_tie += (uint32_t)__popc(be);
-        run_sel += (uint32_t)__popc(bs);
+    for (int base = lo; base < hi; base += 128) {
+        uint32_t k4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * 32 + lane;
+            k4[u] = i < hi ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * 32 + lane;
+            const bool in = i < hi;
+            const bool e = in && k4[u] == T, gsel = in && k4[u] > T;
+            const uint32_t be = __ballot_sync(0xFFFFFFFFu, e);
+            const uint32_t tie_rank = run_tie + (uint32_t)__popc(be & lanemask_lt());
+            const bool sel = gsel || (e && tie_rank < take_me);
+            const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
+            if (sel) out_row[out_base + run_sel + (uint32_t)__popc(bs & lanemask_lt())] = range_start + i;
+            run_tie += (uint32_t)__popc(be);
+            run_sel += (uint32_t)__popc(bs);
+        }
     }
 }
 
@@ -239,18 +472,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const IndexerParams p) {
     using Cfg = IdxCfg<HI, DI, QB, FP8>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled operand tiles
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte alignment for the swizzled operand tiles, by pointer arithmetic on the shared array (an
+    // integer round trip would hide from the compiler that the derived pointers are shared, turning every
+    // access into a slower generic one)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int S = p.stages;
     uint8_t* a_tiles = smem;                                   // S * kStageBytes
     uint8_t* q_tile = a_tiles + (size_t)S * Cfg::kStageBytes;  // kQBytes
     uint32_t* keys = reinterpret_cast<uint32_t*>(q_tile + Cfg::kQBytes);  // QB * chunk
     float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
-    int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64
-    uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + p.chunk / kPage);  // QB x 256
-    uint32_t* allh = hist0 + QB * 256;                                      // 2 x C x 256
-    SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + 2 * cluster_nctarank() * 256);
-    CtrlSmem* ctl = reinterpret_cast<CtrlSmem*>((reinterpret_cast<uintptr_t>(sel + 1) + 15) & ~uintptr_t(15));
+    int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64, padded to 16 bytes
+    // everything after the page list is read with 16-byte vector loads: keep it 16-byte aligned
+    uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + page_words(p.chunk));  // QB x 256
+    uint32_t* allh = hist0 + QB * 256;                                      // C x 768 (select exchange)
+    SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + 3 * cluster_nctarank() * 256);
+    uint8_t* ctl_raw = reinterpret_cast<uint8_t*>(sel + 1);
+    CtrlSmem* ctl = reinterpret_cast<CtrlSmem*>(ctl_raw + ((16u - (smem_u32(ctl_raw) & 15u)) & 15u));
 
     // the attention kernel queued behind this one may be scheduled now: it waits on the device before it
     // reads the Top-K this kernel writes
@@ -508,7 +745,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- cluster-wide Top-K per query -------------------------------------------------------------------
     for (int q = 0; q < nq; ++q) {
         const int64_t visible = (int64_t)L - n_b + j0 + q + 1;
-        cluster_select(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, n_keys, p.top_k, visible,
+        // the smem stage ring is idle once every CTA has scored: it holds the select's fallback exchange space
+        cluster_select(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, reinterpret_cast<uint32_t*>(a_tiles),
+                       n_keys, p.top_k, visible,
                        p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel);
     }
     // No cluster barrier here: every remote access is a histogram push, and the pushes of a pass complete
@@ -519,7 +758,7 @@ template <int HI, int DI, int QB, bool FP8>
 size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
     using Cfg = IdxCfg<HI, DI, QB, FP8>;
     return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
-           (size_t)(chunk / kPage) * 4 + (size_t)(QB + 2 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
+           (size_t)page_words(chunk) * 4 + (size_t)(QB + 3 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
            64;
 }
 

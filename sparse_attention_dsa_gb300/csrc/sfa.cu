@@ -133,7 +133,9 @@ __device__ __forceinline__ int part_slot(int a, int dvh) {
 __global__ void __launch_bounds__(kThreadsSfa, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte alignment by pointer arithmetic on the shared array (an integer round trip would hide from
+    // the compiler that the derived pointers are shared, turning every access into a slower generic one)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* q_s = smem;                         // Q atoms 0-3: [atom][128 rows][128 B]
     uint8_t* kbuf = q_s + kQBytes;               // 2 x K part: [slot][64 rows][128 B]
     uint8_t* vbuf = kbuf + 2 * kKBufBytes;       // 2 x V part

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gen import f32_to_bf16
+from gen import bf16_to_f32, f32_to_bf16
 from gen.workloads import config, make_workload
 
 from _gpu import DeviceWorkload, check_attention, check_topk, ensure_built
@@ -122,6 +122,42 @@ def test_sfa_hand_example_on_device():
     np.testing.assert_allclose(out[0, :, :2], [[0.5, 3.0], [1.0, 2.0]], rtol=0, atol=1e-2)
     assert np.all(out[0, :, 2:] == 0)
     np.testing.assert_allclose(lse[0], [math.log(4), math.log(2)], rtol=0, atol=1e-3)
+
+
+def test_topk_all_scores_tied_takes_lowest_positions():
+    """Every position scores the same, so far more keys share every prefix than the select's candidate
+    exchange holds and the exchanged per-byte passes run.  Ties are taken in ascending position order."""
+    wl = make_workload("ties", 11, [5000], [1], idx_heads=64, idx_dim=128, idx_fp8=False, top_k=512,
+                       attn_heads=128)
+    wl.k_cache[:] = wl.k_cache[wl.page_table[0, 0], 0]
+    scores = oracle.index_scores(wl, 0)
+    assert np.all(scores == scores[0])
+    dw = DeviceWorkload(wl).fused()
+    assert dw.error_word() == 0
+    topk = dw.topk_host()
+    check_topk(wl, topk)
+    assert topk[0].tolist() == list(range(512))
+    out, lse = dw.out_host()
+    check_attention(wl, topk, out, lse)
+
+
+def test_topk_scale_jump_across_the_context():
+    """The second half of the context scores 16x higher (its indexer keys scaled exactly by 16), so the
+    CTAs that score the first half guess the wrong top byte for the K-th key and the select runs its
+    exchanged second-byte pass."""
+    wl = make_workload("jump", 12, [8192], [1], idx_heads=64, idx_dim=128, idx_fp8=False, top_k=2048,
+                       attn_heads=128)
+    for lp in range(64, 128):
+        pg = wl.page_table[0, lp]
+        wl.k_cache[pg] = f32_to_bf16(bf16_to_f32(wl.k_cache[pg]) * np.float32(16.0))
+    scores = oracle.index_scores(wl, 0)
+    assert np.median(scores[4096:]) > 8 * np.median(scores[:4096])
+    dw = DeviceWorkload(wl).fused()
+    assert dw.error_word() == 0
+    topk = dw.topk_host()
+    check_topk(wl, topk)
+    out, lse = dw.out_host()
+    check_attention(wl, topk, out, lse)
 
 
 def test_page_permutation_gives_identical_results():
