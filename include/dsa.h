@@ -93,10 +93,13 @@ const char* dsa_status_string(dsa_status_t status);
 const char* dsa_last_error_message(void);
 
 /*
- * Bytes of device workspace the compute calls need for `dims` (at least 256: the error word plus
- * padding).  The caller allocates it once, zero-fills it before first use, and passes the same
- * buffer to later calls; the error word latches until dsa_clear_device_error().  Returns 0 when dims
- * is NULL.  Calls that may overlap on the GPU need separate workspaces.
+ * Bytes of device workspace the compute calls need for `dims`: 256 bytes whose first int32 is the
+ * device error word, then (when the attention kernel may split one query's positions across several
+ * CTAs: few query tokens) scratch for merging those splits, 129 KiB per CTA of the largest grid it may
+ * use (at most about 33 MiB).  The caller allocates it once (16-byte aligned, as from cudaMalloc),
+ * zero-fills at least the first 256 bytes before first use, and passes the same buffer to later calls;
+ * the error word latches until dsa_clear_device_error().  Returns 0 when dims is NULL.  Calls that may
+ * overlap on the GPU need separate workspaces.
  */
 size_t dsa_workspace_size(const dsa_dims_t* dims);
 
@@ -157,9 +160,9 @@ dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const f
  * another runtime that owns all device memory (a pooled allocator or a server that forbids raw
  * cudaMalloc), decode loops that must not allocate after start-up, and plug-in hosts that offer no
  * allocator.  The kernels are those of dsa_indexer_topk and so are the arguments, except:
- *   - the scratch (the device error word) lives in a static device array of 4096 bytes inside the
- *     library; every GPU that loads the library holds it until the process exits.  Dims whose
- *     dsa_workspace_size() exceeds 4096 bytes are rejected with DSA_ERR_UNSUPPORTED;
+ *   - the scratch (the device error word: the indexer uses only the first 256 bytes of a workspace)
+ *     lives in a static device array of 4096 bytes inside the library; every GPU that loads the
+ *     library holds it until the process exits;
  *   - device_error (optional DEVICE pointer to one int32, may be NULL) receives this call's device
  *     error word (see dsa_get_device_error) on `stream` after the kernel.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that

@@ -289,6 +289,7 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
     p.kv_dim = d->kv_dim;
     p.v_dim = d->v_dim;
     p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
+    p.merge = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kErrorWordArea);
     L.smem_limit = dev.smem_optin;
     L.num_sms = dev.num_sms;
     L.after_indexer = after_indexer;
@@ -331,7 +332,13 @@ const char* dsa_status_string(dsa_status_t s) {
 
 const char* dsa_last_error_message(void) { return g_last_error.c_str(); }
 
-size_t dsa_workspace_size(const dsa_dims_t* dims) { return dims ? 256 : 0; }
+size_t dsa_workspace_size(const dsa_dims_t* dims) {
+    if (!dims) return 0;
+    // the error word area, then the attention kernel's split-merge scratch for the largest grid it may use
+    const int64_t T = dims->total_q > 0 ? dims->total_q : 0;
+    const int32_t K = dims->top_k > 0 ? dims->top_k : 0;
+    return dsa::kErrorWordArea + dsa::sfa_merge_ctas(T, K) * dsa::kSfaMergeFloatsPerCta * sizeof(float);
+}
 
 dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
                               const void* k_cache, const float* k_scale, const int32_t* page_table,

@@ -71,6 +71,7 @@ struct SfaParams {
     float scale_log2;  // softmax_scale * log2(e)
     int32_t splits;    // position splits per query (filled in by the launcher)
     int32_t early_setup;  // launched right behind this library's indexer: only topk comes from it
+    float* merge;         // split-merge scratch: sfa_merge_floats_per_cta() floats per CTA of the grid
 };
 
 struct SfaLaunch {
@@ -82,6 +83,17 @@ struct SfaLaunch {
 };
 
 cudaError_t launch_sfa(const SfaLaunch& launch, cudaStream_t stream);
+
+// Split-merge scratch of the attention kernel: each CTA of a grid with position splits owns one region
+// of kSfaMergeRows partial O rows (256 fp32 each; P * ceil(128 / P) of them are used) and 128
+// (max, sum) pairs.
+constexpr int kSfaMergeRows = 136;
+constexpr size_t kSfaMergeFloatsPerCta = (size_t)kSfaMergeRows * 256 + 2 * 128;
+// The largest grid (in CTAs) the attention launcher can choose with position splits for these sizes
+// (0 when it never splits): at most 256 SMs' worth, or more when top_k forces splits.
+size_t sfa_merge_ctas(int64_t total_q, int32_t top_k);
+// Bytes of workspace the library uses: the 256-byte error word area, plus the attention merge scratch.
+constexpr size_t kErrorWordArea = 256;
 
 // Sets the message returned by dsa_last_error_message() on this host thread.
 void set_last_error(const char* message);

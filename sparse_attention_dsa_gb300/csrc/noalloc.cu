@@ -65,11 +65,9 @@ extern "C" dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const vo
         dsa::set_last_error("dims is NULL");
         return DSA_ERR_INVALID_ARG;
     }
-    const size_t need = dsa_workspace_size(dims);
-    if (need > kStaticScratchBytes) {
-        dsa::set_last_error("dsa_indexer_topk_static: these dims need more scratch than the static array holds");
-        return DSA_ERR_UNSUPPORTED;
-    }
+    // the indexer uses only the error word area of a workspace (the rest is the attention kernel's)
+    const size_t need = dsa::kErrorWordArea;
+    static_assert(dsa::kErrorWordArea <= kStaticScratchBytes, "the static array holds the indexer's scratch");
     void* scratch = nullptr;
     dsa_status_t st = scratch_address(&scratch);
     if (st != DSA_OK) return st;

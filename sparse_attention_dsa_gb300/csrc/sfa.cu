@@ -61,7 +61,6 @@ constexpr int kVBufBytes = 4 * kAtomBytes;
 constexpr int kMaxEntries = 2048;  // selected entries per CTA (per position split)
 constexpr int kEntPerThread = (kMaxEntries + kThreadsSfa - 1) / kThreadsSfa;
 constexpr int kMaxSplits = 8;
-constexpr int kMlRows = 128 + kMaxSplits;  // P * ceil(128 / P) rows at most
 constexpr int kOCols = 256;        // TMEM columns [0, 256): O (this CTA's value half)
 constexpr int kSCol = 256;         // [256, 320): S
 constexpr int kPCol = 320;         // [320, 352): P, 64 bf16 per row
@@ -79,10 +78,10 @@ struct SfaCtrl {
     uint64_t s_full, s_empty;
     uint64_t p_full, p_empty;
     uint64_t mma_done;
+    uint64_t merge_full;  // split merge: the other splits' rows of this CTA have landed in smem
     uint32_t tmem_base;
     int32_t q_waited;
     int32_t tok_b, tok_cu0, tok_cu1;  // sequence of this CTA's query token and its query offsets
-    float2 ml[kMlRows];  // split merge: (max, sum) of the rows pushed to this CTA
 };
 
 constexpr size_t kSfaSmem =
@@ -207,6 +206,7 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
         mbar_init(&ctl->p_full, 4);
         mbar_init(&ctl->p_empty, 1);
         mbar_init(&ctl->mma_done, 1);
+        mbar_init(&ctl->merge_full, 1);
         ctl->q_waited = 0;
         fence_mbar_init();
     }
@@ -513,119 +513,151 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
                 p.lse[(int64_t)t * p.heads + h] = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
     } else {
-        // Merge the P position splits of this value half.  Split j owns head rows [j*slice, (j+1)*slice).
-        // Every CTA pushes each of its O rows, with that row's (max, sum), into the owner's shared memory
-        // (fire-and-forget DSMEM stores); after one cluster barrier each owner combines its rows locally.
-        // Receive buffer (over the Q and K-part buffers): row j*slice + r, 1 KiB of fp32 with its 16-byte
-        // chunks XOR-swizzled by the row, holds split j's partial O of the owner's head ps*slice + r.
+        // Merge the P position splits of this value half through L2.  Split o owns the head rows
+        // [o*slice, (o+1)*slice).  Every CTA stages the rows other splits own in its shared memory (16-byte
+        // chunks swizzled by row), sends each owner its rows with one bulk copy into this CTA's region of
+        // the workspace, and writes the (max, sum) of its rows there.  After one cluster barrier each owner
+        // pulls its rows from every other split with one bulk copy per split and combines them with its own
+        // O, read straight from TMEM.  (An exchange through distributed shared memory was measured at ~10
+        // bytes/cycle per SM here, several times slower; per-row stores or copies issue too slowly.)
         const int slice = (128 + P - 1) / P;
-        float* obuf = reinterpret_cast<float*>(q_s);
-        cluster_sync();  // every CTA of the cluster is past its main loop: the Q and K buffers are free
+        const int rows_here = max(0, min(slice, p.heads - ps * slice));
+        float* my_region = p.merge + (size_t)blockIdx.x * kSfaMergeFloatsPerCta;  // [o*slice + r][256], then ml
+        float2* my_ml = reinterpret_cast<float2*>(my_region + kSfaMergeRows * 256);
+        const int cta0 = (int)blockIdx.x - 2 * ps;  // CTA of split 0 for this token and value half
+        uint8_t* stage = q_s;  // row (o*slice + r) at (o*slice + r) KiB, chunk q at (q ^ (r & 7)) * 16
         if (softmax_thread) {
-            const int owner = h / slice, r = h % slice;
-            const int R = ps * slice + r;  // row in the owner's receive buffer
-            const uint32_t local_row = smem_u32(obuf) + R * 1024;
-            const bool remote = owner != ps;
-            const uint32_t dst = (uint32_t)(dvh + 2 * owner);
-            const uint32_t row_addr = remote ? mapa_shared(local_row, dst) : local_row;
-            const uint32_t ml_local = smem_u32(&ctl->ml[R]);
-            if (remote)
-                asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(mapa_shared(ml_local, dst)), "f"(m_used),
-                             "f"(l_sum)
-                             : "memory");
-            else
-                ctl->ml[R] = make_float2(m_used, l_sum);
+            my_ml[h] = make_float2(m_used, l_sum);
+            const int o = h / slice, r = h - o * slice;
+            const bool send = o != ps && h < p.heads;
+            if (__any_sync(0xFFFFFFFFu, send)) {
+                const uint32_t row = smem_u32(stage) + (uint32_t)h * 1024u;
 #pragma unroll 1
-            for (int c = 0; c < kOCols / 16; c += 4) {
-                float o[4][16];
+                for (int c = 0; c < kOCols / 16; c += 4) {
+                    float v4[4][16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) tmem_ld16(trow + (c + u) * 16, o[u]);
-                tmem_ld_wait();
+                    for (int u = 0; u < 4; ++u) tmem_ld16(trow + (c + u) * 16, v4[u]);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 4; ++u) tmem_regs_ready(o[u]);
+                    for (int u = 0; u < 4; ++u) tmem_regs_ready(v4[u]);
+                    if (send) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float* v = &o[q >> 2][4 * (q & 3)];
-                    const int qc = c * 4 + q;  // 16-byte chunk 0..63
-                    const uint32_t a = row_addr + ((qc ^ (R & 7)) << 4);
-                    if (remote)
-                        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[0]), "f"(v[1]),
-                                     "f"(v[2]), "f"(v[3])
-                                     : "memory");
-                    else
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[0]), "f"(v[1]), "f"(v[2]),
-                                     "f"(v[3])
-                                     : "memory");
+                        for (int q = 0; q < 16; ++q) {
+                            const float* v = &v4[q >> 2][4 * (q & 3)];
+                            const int qc = c * 4 + q;
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((qc ^ (r & 7)) << 4)),
+                                         "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3])
+                                         : "memory");
+                        }
+                    }
                 }
             }
         }
-        __syncthreads();  // the threads with nothing to push wait here rather than in the cluster barrier
-        cluster_sync();  // all pushes have landed
-        // per row of the slice: the weight of every split, exp2(m_j - M) / sum_j l_j exp2(m_j - M), and lse
-        float* wgt = reinterpret_cast<float*>(rows_s);  // [kMaxSplits][slice]; the row list is no longer needed
-        if (tid < slice) {
-            const int r = tid;
-            float M = -INFINITY;
-            for (int j = 0; j < P; ++j) {
-                const float2 v = ctl->ml[j * slice + r];
-                if (v.y > 0.f) M = fmaxf(M, v.x);
-            }
-            float Lsum = 0.f;
-            for (int j = 0; j < P; ++j) {
-                const float2 v = ctl->ml[j * slice + r];
-                if (v.y > 0.f) Lsum += v.y * exp2f(v.x - M);
-            }
-            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            for (int j = 0; j < P; ++j) {
-                const float2 v = ctl->ml[j * slice + r];
-                // a split with no selected row adds nothing (and its O is never read)
-                wgt[j * slice + r] = v.y > 0.f ? exp2f(v.x - M) * inv : 0.f;
-            }
-            const int hh = ps * slice + r;
-            if (dvh == 0 && hh < p.heads && p.lse)
-                p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-        }
+        fence_proxy_async_smem();  // the staged rows are read by the bulk copies (async proxy)
         __syncthreads();
-        // combine: every thread takes (row, 16-byte chunk) items of this CTA's slice, three at a time so
-        // their shared-memory loads overlap
-        const int rows_here = min(slice, p.heads - ps * slice);
-        const int n_items = rows_here * 64;
-        const uint32_t obuf_base = smem_u32(obuf), wgt_base = smem_u32(wgt);
-        for (int idx0 = tid; idx0 < n_items; idx0 += 3 * kThreadsSfa) {
-            float4 acc[3];
-#pragma unroll
-            for (int u = 0; u < 3; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < P; ++j) {
-#pragma unroll
-                for (int u = 0; u < 3; ++u) {
-                    const int idx = idx0 + u * kThreadsSfa;
-                    const int r = (idx < n_items ? idx : 0) >> 6, qc = idx & 63;
-                    const int R = j * slice + r;
-                    float wj;
-                    float4 o;
-                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(wj) : "r"(wgt_base + (uint32_t)(j * slice + r) * 4u));
-                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                 : "=f"(o.x), "=f"(o.y), "=f"(o.z), "=f"(o.w)
-                                 : "r"(obuf_base + (uint32_t)R * 1024u + ((uint32_t)(qc ^ (R & 7)) << 4)));
-                    // a split with no selected row has weight 0 and an O that is never written: select, not scale
-                    const bool use = wj != 0.f;
-                    acc[u].x += use ? o.x * wj : 0.f;
-                    acc[u].y += use ? o.y * wj : 0.f;
-                    acc[u].z += use ? o.z * wj : 0.f;
-                    acc[u].w += use ? o.w * wj : 0.f;
-                }
+        if (tid == 0) {
+            for (int o = 0; o < P; ++o) {
+                const int n = max(0, min(slice, p.heads - o * slice));
+                if (o == ps || n == 0) continue;
+                bulk_copy_s2g(my_region + (size_t)o * slice * 256, stage + (size_t)o * slice * 1024, (uint32_t)n * 1024u);
             }
-#pragma unroll
-            for (int u = 0; u < 3; ++u) {
-                const int idx = idx0 + u * kThreadsSfa;
-                if (idx >= n_items) continue;
-                const int r = idx >> 6, qc = idx & 63;
-                const uint2 pk = make_uint2(f2_to_bf2(acc[u].x, acc[u].y), f2_to_bf2(acc[u].z, acc[u].w));
-                *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + ps * slice + r) * kVDim + dvh * kOCols + qc * 4) =
-                    pk;
+            bulk_commit_and_wait();  // written to global memory (and the staging may be reused)
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        cluster_sync();  // every split's rows and (max, sum) are visible
+        // this CTA's rows from every other split, row j*slice + r, same swizzle
+        uint8_t* obuf = q_s;
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t bytes = (uint32_t)((P - 1) * rows_here * 1024);
+            if (bytes > 0) {
+                mbar_arrive_expect_tx(&ctl->merge_full, bytes);
+                for (int j = 0; j < P; ++j) {
+                    if (j == ps) continue;
+                    bulk_copy_g2s(obuf + (size_t)j * slice * 1024,
+                                  p.merge + (size_t)(cta0 + 2 * j) * kSfaMergeFloatsPerCta + (size_t)ps * slice * 256,
+                                  (uint32_t)rows_here * 1024u, &ctl->merge_full);
+                }
+            } else {
+                mbar_arrive(&ctl->merge_full);
             }
         }
-        // no DSMEM access follows the second barrier, so a CTA may exit as soon as its own rows are written
+        // Combine: the three warps of each TMEM lane quadrant (one softmax warp, two gather warps) share the
+        // 16 column chunks of that quadrant's rows.
+        if (warp >= 2) {
+            const int quad = warp & 3, part = (warp - 2) >> 2;  // part 0..2 within the quadrant
+            const int hh = quad * 32 + lane, r = hh - ps * slice;
+            const bool own_row = r >= 0 && r < rows_here;
+            if (__any_sync(0xFFFFFFFFu, own_row)) {
+                const uint32_t tr = tmem + (((uint32_t)quad * 32u) << 16);
+                // weights of the splits for this row: exp2(m_j - M) / sum_j l_j exp2(m_j - M)
+                float2 ml[kMaxSplits];
+                float M = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kMaxSplits; ++j) {
+                    ml[j] = make_float2(-INFINITY, 0.f);
+                    if (j < P && own_row)
+                        ml[j] = __ldcg(reinterpret_cast<const float2*>(p.merge + (size_t)(cta0 + 2 * j) *
+                                                                       kSfaMergeFloatsPerCta + kSfaMergeRows * 256) + hh);
+                    if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
+                }
+                float wj[kMaxSplits], Lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < kMaxSplits; ++j) {
+                    wj[j] = ml[j].y > 0.f ? exp2f(ml[j].x - M) : 0.f;
+                    Lsum += ml[j].y * wj[j];
+                }
+                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+                float w_own = 0.f;
+#pragma unroll
+                for (int j = 0; j < kMaxSplits; ++j) {
+                    wj[j] *= inv;
+                    if (j == ps) w_own = wj[j];
+                }
+                if (part == 0 && own_row && dvh == 0 && p.lse)
+                    p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+                const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->merge_full, 0, p.err));
+                const int c_lo = part == 0 ? 0 : (part == 1 ? 6 : 11), c_hi = part == 0 ? 6 : (part == 1 ? 11 : 16);
+#pragma unroll 1
+                for (int c = c_lo; c < c_hi; ++c) {
+                    float o[16];
+                    tmem_ld16(tr + c * 16, o);
+                    tmem_ld_wait();
+                    tmem_regs_ready(o);
+                    if (own_row && got) {
+                        float acc[16];
+                        // a split with no selected row has weight 0 and an O that is never read: select, not scale
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) acc[k] = w_own != 0.f ? o[k] * w_own : 0.f;
+#pragma unroll
+                        for (int j = 0; j < kMaxSplits; ++j) {
+                            if (j >= P || j == ps || wj[j] == 0.f) continue;
+                            const uint32_t rowp = smem_u32(obuf) + (uint32_t)(j * slice + r) * 1024u;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                float4 v;
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                             : "r"(rowp + (((c * 4 + k) ^ (r & 7)) << 4)));
+                                acc[4 * k] += v.x * wj[j];
+                                acc[4 * k + 1] += v.y * wj[j];
+                                acc[4 * k + 2] += v.z * wj[j];
+                                acc[4 * k + 3] += v.w * wj[j];
+                            }
+                        }
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) pk[k] = f2_to_bf2(acc[2 * k], acc[2 * k + 1]);
+                        uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)t * p.heads + hh) * kVDim + dvh * kOCols + c * 16);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+            }
+        }
+        // every bulk copy into this CTA has landed before it exits (the combining warps saw the barrier;
+        // a CTA without owned rows waits here)
+        if (tid == 0) mbar_wait(&ctl->merge_full, 0, p.err);
     }
     tc_fence_before();
     __syncthreads();
@@ -634,6 +666,22 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
 }
 
 }  // namespace
+
+// Position splits P (a cluster of 2P CTAs per query token): the fewest that keep a split within
+// kMaxEntries entries, grown while the grid still fits on `sms` SMs.
+static int splits_for(int64_t total_q, int top_k, int sms) {
+    int P = 1;
+    while (P < kMaxSplits && (top_k + P - 1) / P > kMaxEntries) ++P;
+    const int max_splits = (top_k + kRows - 1) / kRows;
+    while (P < kMaxSplits && P + 1 <= max_splits && total_q * 2 * (P + 1) <= sms) ++P;
+    return P;
+}
+
+size_t sfa_merge_ctas(int64_t total_q, int32_t top_k) {
+    // the launcher never counts more than 256 SMs, so this grid bounds the one it picks
+    const int P = splits_for(total_q, top_k, 256);
+    return P > 1 ? (size_t)total_q * 2 * P : 0;
+}
 
 // Clusters of `size` CTAs of this kernel that can be resident at once (cached per device and size).
 static int max_active_clusters(int size) {
@@ -665,22 +713,20 @@ static int max_active_clusters(int size) {
 
 cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
     SfaParams p = L.params;
-    static_assert(kQBytes + 2 * kKBufBytes >= kMlRows * 1024, "split merge buffer must fit in the Q and K-part buffers");
+    static_assert(kQBytes + 2 * kKBufBytes >= kSfaMergeRows * 1024, "split merge rows must fit in the Q and K-part buffers");
+    static_assert(kSfaMergeRows >= 128 + kMaxSplits - 1, "P * ceil(128 / P) rows at most");
     if (kSfaSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSfaSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    // Position splits P (a cluster of 2P CTAs per query token): the fewest that keep a split within
-    // kMaxEntries entries, grown while the CTAs still fit on the SMs, then shrunk until every cluster
-    // of the grid can be resident at once (a second wave of clusters would double the time).
-    int P = 1;
-    while (P < kMaxSplits && (p.top_k + P - 1) / P > kMaxEntries) ++P;
+    // Position splits: grown while the CTAs still fit on the SMs, then shrunk until every cluster of the
+    // grid can be resident at once (a second wave of clusters would double the time).
+    int P = splits_for(p.total_q, p.top_k, L.num_sms < 256 ? L.num_sms : 256);
     if ((p.top_k + P - 1) / P > kMaxEntries) return cudaErrorInvalidValue;
-    const int min_p = P;
-    const int max_splits = (p.top_k + kRows - 1) / kRows;
-    while (P < kMaxSplits && P + 1 <= max_splits && (int64_t)p.total_q * 2 * (P + 1) <= L.num_sms) ++P;
+    const int min_p = splits_for(p.total_q, p.top_k, 0);
     while (P > min_p && P > 1 && p.total_q > max_active_clusters(2 * P)) --P;
+    if (P > 1 && (size_t)p.total_q * 2 * P > sfa_merge_ctas(p.total_q, p.top_k)) return cudaErrorInvalidValue;
     p.splits = P;
     p.early_setup = L.after_indexer ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
