@@ -145,14 +145,27 @@ dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* 
                              float* lse, void* workspace, void* stream);
 
 /*
- * The whole decode/prefill step: dsa_indexer_topk followed by dsa_sparse_attn on the same stream
- * ([A2] "Fusing Index Screening with Multi-Stream Orchestration"; [A4] 3.1-3.2).  topk_idx is an
- * output (the selection used by the attention).  Arguments and limits are those of the two calls.
+ * The whole decode/prefill step: the work of dsa_indexer_topk followed by that of dsa_sparse_attn on
+ * the same stream ([A2] "Fusing Index Screening with Multi-Stream Orchestration"; [A4] 3.1-3.2).
+ * topk_idx is an output (the selection used by the attention).  Arguments and limits are those of the
+ * two calls.  When every sequence has exactly one query token and both stages fit one thread-block
+ * cluster per token (64 indexer heads of 128 dims), this is ONE kernel launch: each cluster scores its
+ * token's context, selects the Top-K and runs the attention.  Otherwise it is the two kernels, the
+ * attention launched as a programmatic dependent of the indexer.  dsa_fused_decode_launches() tells
+ * which.
  */
 dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
                               const void* k_cache, const float* k_scale, const void* q, const void* kv_cache,
                               const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
                               int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream);
+
+/*
+ * Kernel launches dsa_fused_decode makes for `dims` on the current device: 1 (the single-launch
+ * kernel), 2 (indexer, then attention), 0 (no query token), or -1 when dims are invalid or unsupported
+ * (the reason is in dsa_last_error_message()).  Host-only: launches nothing.  The articles have no
+ * counterpart to this call.
+ */
+int32_t dsa_fused_decode_launches(const dsa_dims_t* dims);
 
 /*
  * dsa_indexer_topk without a workspace argument.  The articles have no counterpart to this call; it

@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     abi_version,
     clear_device_error,
     fused_decode,
+    fused_decode_launches,
     get_device_error,
     indexer_topk,
     indexer_topk_static,

@@ -26,6 +26,7 @@ EXPORTED = (
     "dsa_indexer_topk",
     "dsa_sparse_attn",
     "dsa_fused_decode",
+    "dsa_fused_decode_launches",
     "dsa_get_device_error",
     "dsa_clear_device_error",
     "dsa_indexer_topk_static",
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.dsa_sparse_attn.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 10
             L.dsa_fused_decode.restype = st
             L.dsa_fused_decode.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 15
+            L.dsa_fused_decode_launches.restype = ctypes.c_int32
+            L.dsa_fused_decode_launches.argtypes = [ctypes.POINTER(DsaDims)]
             L.dsa_get_device_error.restype = st
             L.dsa_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
             L.dsa_clear_device_error.restype = st
@@ -155,6 +158,14 @@ def fused_decode(dims, q_idx, q_scale, w, k_cache, k_scale, q, kv_cache, page_ta
                                   _ptr(k_scale), _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),
                                   _ptr(cu_q_lens), _ptr(topk_idx), _ptr(out), _ptr(lse), _ptr(workspace),
                                   _stream(stream)))
+
+
+def fused_decode_launches(dims) -> int:
+    """Kernel launches fused_decode makes for these dims on the current device (1, 2, or 0)."""
+    n = int(lib().dsa_fused_decode_launches(ctypes.byref(dims)))
+    if n < 0:
+        raise DsaError(DSA_ERR_INVALID_ARG, lib().dsa_last_error_message().decode())
+    return n
 
 
 def indexer_topk_static(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx,

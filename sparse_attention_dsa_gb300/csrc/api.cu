@@ -205,9 +205,12 @@ dsa_status_t encode_indexer_maps(const dsa_dims_t* d, const void* q_idx, const v
     return DSA_OK;
 }
 
-dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_scale, const float* w,
-                         const void* k_cache, const float* k_scale, const int32_t* page_table, const int32_t* seq_lens,
-                         const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace, void* stream) {
+// Everything of an indexer call but the launch.  *launch is false when there is nothing to launch.
+dsa_status_t prepare_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_scale, const float* w,
+                             const void* k_cache, const float* k_scale, const int32_t* page_table,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace,
+                             dsa::IndexerLaunch* Lout, bool* launch) {
+    *launch = false;
     dsa_status_t st = check_common(d);
     if (st) return st;
     const bool fp8 = d->idx_dtype == DSA_FP8_E4M3;
@@ -219,7 +222,7 @@ dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_
     if (fp8 && ((st = check_ptr(q_scale, "q_scale")) || (st = check_ptr(k_scale, "k_scale")))) return st;
     DeviceInfo dev;
     if ((st = device_info(&dev))) return st;
-    dsa::IndexerLaunch L;
+    dsa::IndexerLaunch& L = *Lout;
     memset(&L, 0, sizeof L);
     if ((st = plan_indexer(d, dev, &L))) return st;
     if (d->total_q == 0) return DSA_OK;
@@ -234,6 +237,11 @@ dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_
     p.cu_q_lens = cu_q_lens;
     p.topk = topk_idx;
     p.err = static_cast<int32_t*>(workspace);
+    *launch = true;
+    return DSA_OK;
+}
+
+dsa_status_t launch_indexer_checked(const dsa::IndexerLaunch& L, void* stream) {
     cudaError_t e = dsa::launch_indexer(L, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidClusterSize)
         return fail(DSA_ERR_UNSUPPORTED, "a cluster of %d CTAs does not fit on this device", L.cluster);
@@ -241,11 +249,22 @@ dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_
     return DSA_OK;
 }
 
-// after_indexer: the previous launch on this stream is this library's indexer, made in the same call on the
-// same inputs, so the attention kernel may start before it ends (it waits on the device for the Top-K).
-dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
-                     const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out, float* lse,
-                     void* workspace, void* stream, bool after_indexer = false) {
+dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_scale, const float* w,
+                         const void* k_cache, const float* k_scale, const int32_t* page_table, const int32_t* seq_lens,
+                         const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace, void* stream) {
+    dsa::IndexerLaunch L;
+    bool launch = false;
+    dsa_status_t st = prepare_indexer(d, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens,
+                                      topk_idx, workspace, &L, &launch);
+    if (st || !launch) return st;
+    return launch_indexer_checked(L, stream);
+}
+
+// Everything of an attention call but the launch.  *launch is false when there is nothing to launch.
+dsa_status_t prepare_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
+                         const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out,
+                         float* lse, void* workspace, dsa::SfaLaunch* Lout, bool* launch) {
+    *launch = false;
     dsa_status_t st = check_common(d);
     if (st) return st;
     if (d->attn_heads < 1) return fail(DSA_ERR_INVALID_ARG, "attn_heads must be >= 1 (got %d)", d->attn_heads);
@@ -268,7 +287,7 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
     DeviceInfo dev;
     if ((st = device_info(&dev))) return st;
     if (d->total_q == 0) return DSA_OK;
-    dsa::SfaLaunch L;
+    dsa::SfaLaunch& L = *Lout;
     memset(&L, 0, sizeof L);
     dsa::SfaParams& p = L.params;
     p.q = static_cast<const uint16_t*>(q);
@@ -292,7 +311,6 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
     p.merge = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kErrorWordArea);
     L.smem_limit = dev.smem_optin;
     L.num_sms = dev.num_sms;
-    L.after_indexer = after_indexer;
     {
         EncodeTiledFn enc = encode_fn();
         if (!enc) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -305,9 +323,28 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "tensor map for q: CUresult %d", (int)r);
     }
+    *launch = true;
+    return DSA_OK;
+}
+
+// after_indexer: the previous launch on this stream is this library's indexer, made in the same call on the
+// same inputs, so the attention kernel may start before it ends (it waits on the device for the Top-K).
+dsa_status_t launch_sfa_checked(dsa::SfaLaunch L, void* stream, bool after_indexer) {
+    L.after_indexer = after_indexer;
     cudaError_t e = dsa::launch_sfa(L, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
     return DSA_OK;
+}
+
+dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
+                     const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out, float* lse,
+                     void* workspace, void* stream) {
+    dsa::SfaLaunch L;
+    bool launch = false;
+    dsa_status_t st =
+        prepare_sfa(d, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, &L, &launch);
+    if (st || !launch) return st;
+    return launch_sfa_checked(L, stream, false);
 }
 
 }  // namespace
@@ -361,12 +398,44 @@ dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const f
                               const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
                               int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream) {
     g_last_error.clear();
-    dsa_status_t st = run_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx,
-                                  workspace, stream);
+    dsa::IndexerLaunch IL;
+    dsa::SfaLaunch SL;
+    bool li = false, ls = false;
+    dsa_status_t st = prepare_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens,
+                                      topk_idx, workspace, &IL, &li);
     if (st) return st;
-    // the indexer was launched on this stream just now whenever there is a query token
-    return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream,
-                   dims->total_q > 0);
+    st = prepare_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, &SL, &ls);
+    if (st) return st;
+    if (!li || !ls) return DSA_OK;  // no query token
+    // one launch when every query token can have a cluster of its own for both phases
+    cudaError_t e = dsa::launch_decode(IL, SL, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) return DSA_OK;
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode launch");
+    // otherwise the indexer, then the attention kernel as its programmatic dependent
+    if ((st = launch_indexer_checked(IL, stream))) return st;
+    return launch_sfa_checked(SL, stream, true);
+}
+
+int32_t dsa_fused_decode_launches(const dsa_dims_t* dims) {
+    g_last_error.clear();
+    if (!dims) {
+        dsa::set_last_error("dims is NULL");
+        return -1;
+    }
+    if (check_common(dims) != DSA_OK) return -1;
+    if (dims->total_q == 0) return 0;
+    DeviceInfo dev;
+    if (device_info(&dev) != DSA_OK) return -1;
+    dsa::IndexerLaunch IL;
+    memset(&IL, 0, sizeof IL);
+    if (plan_indexer(dims, dev, &IL) != DSA_OK) return -1;
+    dsa::SfaLaunch SL;
+    memset(&SL, 0, sizeof SL);
+    SL.params.total_q = dims->total_q;
+    SL.params.top_k = dims->top_k;
+    SL.num_sms = dev.num_sms;
+    SL.smem_limit = dev.smem_optin;
+    return dsa::decode_single_launch(IL, SL) ? 1 : 2;
 }
 
 dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* code) {

@@ -1,765 +1,22 @@
-// Fused lightning indexer + Top-K for sm_103a.
-//
-// Computes, for every query token t, I[t,s] = sum_h w[t,h] * max(0, q_idx[t,h,:] . k[s,:]) over the
-// visible positions s <= p_t, and writes only the K best positions ("Optimizing Inference for Hybrid
-// Attention Architectures: From Operator Fusion to Sequence Sharding", section "Breaking Down the
-// Computational Path of Hybrid Attention", step 1; "Day0 Inference Optimization for Next-Generation
-// Hybrid-Architecture LLMs Based on CANN", section 2.1: scoring, head weighting and Top-K fused in one
-// kernel that reads the paged K cache; "Day0 Inference Support and Performance Optimization for New LLM
-// Architectures", section 3.1: no score tensor leaves the chip).
-//
-// Work decomposition: one thread-block cluster of C CTAs per (sequence, block of up to QB query tokens).
-// CTA r of the cluster scores positions [r*chunk, (r+1)*chunk) of that sequence and keeps the scores as
-// order-preserving uint32 keys in its own shared memory.  A cluster-wide radix select (8-bit digits,
-// most significant first; histograms and, for the last two bytes, the surviving candidate keys
-// exchanged through distributed shared memory, usually in two rounds) then finds the K-th key, and
-// every CTA writes its selected positions in ascending order at an offset derived from the per-CTA
-// counts.
-//
-// Scoring pipeline inside a CTA (warp-specialised):
-//   warp 0  : TMA producer.  Each 128-position tile is two 64-token pages of the indexer K cache,
-//             fetched with 3-D tensor-map loads (page id from the page table) into 128B-swizzled smem.
-//   warp 1  : tcgen05 issuer.  D[128 positions, N] = K_tile[128, Di] * Qblk[N, Di]^T with
-//             N = QB*Hi (padded to 16), accumulated in fp32 in tensor memory (two buffers).
-//   warps 2-5: epilogue.  Each thread owns one TMEM lane (= one position), reads its N columns and
-//             reduces sum_h w*max(0, acc) per query (FP8: times the key row scale), then stores the key.
-//   warps 6-7: idle during scoring; all 8 warps run the selection.
+// The standalone indexer kernel (one launch per dsa_indexer_topk call) and its launcher.  The device
+// code lives in indexer_impl.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "indexer_impl.cuh"
 
 namespace dsa {
 namespace {
-
-constexpr int kThreads = 256;
-constexpr int kTileM = 128;  // positions per tile (two pages)
-constexpr int kPage = 64;
-constexpr int kMaxCluster = 16;
-
-template <int HI, int DI, int QB, bool FP8>
-struct IdxCfg {
-    static constexpr int kNReal = HI * QB;
-    static constexpr int kN = kNReal < 16 ? 16 : ((kNReal + 15) / 16) * 16;  // UMMA N for M = 128
-    static constexpr int kElem = FP8 ? 1 : 2;
-    static constexpr int kRowBytes = DI * kElem;
-    static constexpr int kAtoms = kRowBytes / 128;  // 128-byte swizzle atoms along K
-    static constexpr int kStageBytes = kTileM * kRowBytes;
-    static constexpr int kQBytes = kN * kRowBytes;
-    static constexpr int kMmaK = FP8 ? 32 : 16;  // elements per UMMA
-    static constexpr int kKSteps = DI / kMmaK;
-    // accumulator buffers in TMEM: enough that the MMA issuer rarely waits for the epilogue
-    static constexpr int kAccBufs = (4 * kN) <= 512 ? 4 : 2;
-    static constexpr int kTmemCols = (kAccBufs * kN) <= 32 ? 32 : (kAccBufs * kN) <= 64 ? 64
-                                     : (kAccBufs * kN) <= 128 ? 128 : (kAccBufs * kN) <= 256 ? 256 : 512;
-    static constexpr uint32_t kIdesc = make_idesc(128, kN, FP8 ? 0u : 1u, FP8 ? 0u : 1u, 0u, 0u);
-    static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
-    // the select's fallback exchange space (2 x C x 256 words) lives in the stage ring (at least 2 stages)
-    static_assert(2 * kStageBytes >= 2 * kMaxCluster * 256 * 4, "stage ring too small for the select");
-    static_assert(kN <= 256, "UMMA N limit");
-    static_assert(QB <= 4, "per-query select state is sized for four queries");
-};
-
-constexpr int kCandCap = 256;  // second-round candidates one CTA may send (a power of two)
-
-// Words of the per-CTA page list: one per 64-position page, rounded up to whole 16-byte units.
-__host__ __device__ constexpr int page_words(int chunk) { return ((chunk / kPage) + 3) & ~3; }
-
-struct SelectSmem {
-    alignas(16) uint32_t hist[2][256];
-    alignas(16) uint32_t totals[256];
-    uint32_t res[8];                 // results broadcast from the warp that finds a boundary bin
-    uint32_t gt[kMaxCluster];        // keys above the boundary found so far, per CTA of the cluster
-    uint32_t ecnt[kMaxCluster];      // keys equal to the K-th key, per CTA
-    uint32_t guess_in[kMaxCluster];  // round A: every CTA's guess of the top byte (pushed by that CTA)
-    uint32_t ncand_in[kMaxCluster];  // round B: every CTA's candidate count (pushed by that CTA)
-    uint32_t scan_e[kThreads / 32];
-    uint32_t scan_s[kThreads / 32];
-    uint32_t ncand;
-    uint32_t take_me;
-    uint32_t off_me;
-};
-
-struct CtrlSmem {
-    uint64_t full[kMaxStages];
-    uint64_t empty[kMaxStages];
-    uint64_t tfull[4];
-    uint64_t tempty[4];
-    uint64_t qbar;
-    uint32_t tmem_base;
-    int32_t consumed;  // tiles consumed by the MMA warp (drain bookkeeping)
-    int32_t issued;    // tiles issued by the producer
-    int32_t qwaited;
-};
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
-// The bin of `totals` (256 bins, ascending key order, 16-byte aligned) that holds the remaining-th largest
-// key, and that key's rank inside the bin.  Called by one warp; every lane gets the result.
-__device__ __forceinline__ void boundary_bin(const uint32_t* totals, uint32_t remaining, uint32_t& bstar,
-                                             uint32_t& rem) {
-    const int lane = threadIdx.x & 31;
-    uint32_t v[8], lsum = 0;
-    {
-        const uint4 a = reinterpret_cast<const uint4*>(totals)[2 * lane];
-        const uint4 b = reinterpret_cast<const uint4*>(totals)[2 * lane + 1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) lsum += v[j];
-    uint32_t incl = lsum;  // keys in the bins at or above lane*8
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, off);
-        if (lane + off < 32) incl += t;
-    }
-    uint32_t above = incl - lsum;
-    uint32_t found = 0, fb = 0, fr = 0;
-#pragma unroll
-    for (int j = 7; j >= 0; --j) {
-        if (above < remaining && remaining <= above + v[j]) {
-            found = 1;
-            fb = (uint32_t)(lane * 8 + j);
-            fr = remaining - above;
-        }
-        above += v[j];
-    }
-    const uint32_t who = __ballot_sync(0xFFFFFFFFu, found != 0);
-    const int src = who ? __ffs(who) - 1 : 0;
-    bstar = __shfl_sync(0xFFFFFFFFu, fb, src);
-    rem = __shfl_sync(0xFFFFFFFFu, fr, src);
-}
-
-// S.gt[r] += the keys of CTA r in bins above bstar (its histogram: ah[r * stride + bin]).
-__device__ __forceinline__ void add_above(const uint32_t* ah, int stride, uint32_t bstar, uint32_t C, SelectSmem& S) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
-        uint32_t s = 0;
-        for (int i = lane; i < 256; i += 32) s += (uint32_t)i > bstar ? ah[r * stride + i] : 0u;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-        if (lane == 0) S.gt[r] += s;
-    }
-}
-
-// One radix pass with a cluster-wide histogram: this CTA's keys that match `prefix` above bit shift+8 are
-// counted by their byte at `shift`, every CTA's histogram is pushed into slot [rank] of `buf` ([C][256]) in
-// every CTA of the cluster, and all CTAs find the same boundary bin.
-__device__ void exchange_pass(const uint32_t* keys, int n, uint32_t prefix, int shift, uint32_t* buf, uint32_t rank,
-                              uint32_t C, uint32_t& remaining, uint32_t& bstar, SelectSmem& S) {
-    const int tid = threadIdx.x;
-    const uint32_t hmask = 0xFFFFFFFFu << (shift + 8);
-    S.hist[0][tid] = 0;
-    __syncthreads();
-    // plain shared atomics: a warp-level match would cost one round per distinct bin
-    for (int i = tid; i < n; i += kThreads) {
-        const uint32_t key = keys[i];
-        if (((key ^ prefix) & hmask) == 0) atomicAdd(&S.hist[0][(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    const uint32_t slot = smem_u32(buf + rank * 256 + tid);
-    for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), S.hist[0][tid]);
-    cluster_sync();
-    uint32_t tot = 0;
-    for (uint32_t r = 0; r < C; ++r) tot += buf[r * 256 + tid];
-    S.totals[tid] = tot;
-    __syncthreads();
-    if (tid < 32) {
-        uint32_t b, rem;
-        boundary_bin(S.totals, remaining, b, rem);
-        if (tid == 0) {
-            S.res[0] = b;
-            S.res[1] = rem;
-        }
-    }
-    __syncthreads();
-    bstar = S.res[0];
-    remaining = S.res[1];
-    add_above(buf, 256, bstar, C, S);
-    __syncthreads();  // S.totals, S.hist and S.res are reused next
-}
-
-// Cluster-wide Top-K of one query: the K largest of the cluster's keys, as positions in ascending order.
-//   keys: this CTA's n keys (position range_start + i); hist0: their top-byte histogram, built while
-//   scoring; allh: C x 768 words of exchange space that nothing but this function touches; sbuf:
-//   2 x C x 256 words of further exchange space that peers may write once every CTA of the cluster has
-//   finished scoring.
-// The K-th key is found radix-fashion, most significant byte first, with two cluster rounds in the usual
-// case: round A exchanges the top-byte histograms together with a second-byte histogram of the bin each
-// CTA guesses will hold the K-th key (the bin where its own count from the top reaches its share of K);
-// when every guess is the agreed top byte, the second byte is settled in the same round.  Round B sends
-// every key that still matches
-// the 16-bit prefix (usually a few dozen per CTA) to every CTA, which finds the exact K-th key among them.
-// A wrong guess or too many candidates falls back to a full exchanged pass per byte.  All CTAs of the
-// cluster call this with identical (K, visible), so the cluster barriers inside match up.
-__device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, uint32_t* sbuf, int n,
-                               int K, int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
-                               SelectSmem& S) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (visible <= K) {  // every visible position is kept: 0..p in order, then -1
-        const int per = (K + (int)C - 1) / (int)C;
-        const int lo = (int)rank * per, hi = min(K, lo + per);
-        for (int s = lo + tid; s < hi; s += kThreads) out_row[s] = (int64_t)s < visible ? s : -1;
-        return;
-    }
-    uint32_t remaining = (uint32_t)K, prefix = 0, bstar = 0;
-    if (tid < kMaxCluster) S.gt[tid] = 0;
-    uint32_t* ahA = allh;             // round A: [C][512] = top-byte | guessed second-byte histograms
-    uint32_t* cand = allh + C * 512;  // round B: [C][kCandCap] candidate keys
-    static_assert(kCandCap <= 256, "round-B candidates share the 768-word slot");
-
-    // ---- round A: the top-byte histogram, and the second-byte histogram of the guessed bin ----
-    if (tid < 32) {
-        uint32_t g, gr;
-        boundary_bin(hist0, (uint32_t)((K + (int)C - 1) / (int)C), g, gr);
-        if (tid == 0) S.res[7] = g;
-    }
-    S.hist[1][tid] = 0;
-    __syncthreads();
-    const uint32_t guess = S.res[7];
-    for (int i0 = 4 * tid; i0 < n; i0 += 4 * kThreads * 8) {
-        uint4 k8[8];  // eight 16-byte loads in flight (n is a multiple of 128)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 4 * kThreads;
-            k8[u] = i < n ? *reinterpret_cast<const uint4*>(keys + i) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t kv[4] = {k8[u].x, k8[u].y, k8[u].z, k8[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (i0 + u * 4 * kThreads < n && (kv[e] >> 24) == guess) atomicAdd(&S.hist[1][(kv[e] >> 16) & 255u], 1u);
-        }
-    }
-    __syncthreads();
-    {
-        const uint32_t slot = smem_u32(ahA + rank * 512 + tid);
-        const uint32_t h0 = hist0[tid], h1 = S.hist[1][tid];
-        for (uint32_t r = 0; r < C; ++r) {
-            const uint32_t a = mapa_shared(slot, r);
-            st_dsmem_u32(a, h0);
-            st_dsmem_u32(a + 256 * 4, h1);
-        }
-        if (tid < (int)C) st_dsmem_u32(mapa_shared(smem_u32(&S.guess_in[rank]), (uint32_t)tid), guess);
-    }
-    cluster_sync();  // also: every CTA of the cluster has finished scoring, so sbuf may now be written
-    {
-        uint32_t t0 = 0, t1 = 0;
-        for (uint32_t r = 0; r < C; ++r) {
-            t0 += ahA[r * 512 + tid];
-            t1 += ahA[r * 512 + 256 + tid];
-        }
-        S.totals[tid] = t0;
-        S.hist[0][tid] = t1;
-    }
-    __syncthreads();
-    if (tid < 32) {
-        uint32_t b0, r0, b1 = 0, r1 = 0;
-        boundary_bin(S.totals, remaining, b0, r0);
-        // the guessed second-byte histograms count the right keys when every CTA guessed this bin
-        const bool agree = __all_sync(0xFFFFFFFFu, lane >= (int)C || S.guess_in[lane] == b0);
-        if (agree) boundary_bin(S.hist[0], r0, b1, r1);
-        if (tid == 0) {
-            S.res[0] = b0;
-            S.res[1] = r0;
-            S.res[2] = agree ? 1u : 0u;
-            S.res[3] = b1;
-            S.res[4] = r1;
-        }
-    }
-    __syncthreads();
-    bstar = S.res[0];
-    remaining = S.res[1];
-    const bool spec = S.res[2] != 0;
-    add_above(ahA, 512, bstar, C, S);
-    prefix = bstar << 24;
-    if (spec) {
-        bstar = S.res[3];
-        remaining = S.res[4];
-        add_above(ahA + 256, 512, bstar, C, S);
-        __syncthreads();  // S.res is reused
-    } else {
-        __syncthreads();
-        exchange_pass(keys, n, prefix, 16, sbuf, rank, C, remaining, bstar, S);
-    }
-    prefix |= bstar << 16;
-
-    // ---- round B: the keys that still match the 16-bit prefix, sent to every CTA ----
-    if (tid == 0) S.ncand = 0;
-    __syncthreads();
-    for (int i0 = 4 * tid; i0 < n; i0 += 4 * kThreads * 8) {
-        uint4 k8[8];  // eight 16-byte loads in flight (n is a multiple of 128)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 4 * kThreads;
-            k8[u] = i < n ? *reinterpret_cast<const uint4*>(keys + i) : make_uint4(0, 0, 0, 0);
-        }
-        // matches are rare: mark them in a mask here, send them from a small rolled loop below (one copy of
-        // the sending code instead of 32)
-        uint32_t mask = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t kv[4] = {k8[u].x, k8[u].y, k8[u].z, k8[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (i0 + u * 4 * kThreads < n && ((kv[e] ^ prefix) & 0xFFFF0000u) == 0) mask |= 1u << (4 * u + e);
-        }
-#pragma unroll 1
-        while (mask != 0) {
-            const int bit = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const uint32_t key = keys[i0 + (bit >> 2) * 4 * kThreads + (bit & 3)];
-            const uint32_t j = atomicAdd(&S.ncand, 1u);
-            if (j < (uint32_t)kCandCap) {
-                const uint32_t slot = smem_u32(cand + rank * kCandCap + j);
-                for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), key);
-            }
-        }
-    }
-    __syncthreads();
-    if (tid < (int)C) st_dsmem_u32(mapa_shared(smem_u32(&S.ncand_in[rank]), (uint32_t)tid), S.ncand);
-    cluster_sync();
-    const bool fits = __syncthreads_and(tid >= (int)C || S.ncand_in[tid] <= (uint32_t)kCandCap) != 0;
-    uint32_t T;
-    if (fits) {
-        // every CTA holds the same candidate set: find the remaining-th largest among them locally
-        S.hist[0][tid] = 0;
-        S.hist[1][tid] = 0;
-        __syncthreads();
-        for (int idx = tid; idx < (int)C * kCandCap; idx += kThreads) {
-            const uint32_t r = (uint32_t)idx / kCandCap, j = (uint32_t)idx % kCandCap;
-            if (j < S.ncand_in[r]) atomicAdd(&S.hist[0][(cand[idx] >> 8) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            uint32_t b2, r2;
-            boundary_bin(S.hist[0], remaining, b2, r2);
-            if (tid == 0) {
-                S.res[0] = b2;
-                S.res[1] = r2;
-            }
-        }
-        __syncthreads();
-        const uint32_t b2 = S.res[0];
-        remaining = S.res[1];
-        for (int idx = tid; idx < (int)C * kCandCap; idx += kThreads) {
-            const uint32_t r = (uint32_t)idx / kCandCap, j = (uint32_t)idx % kCandCap;
-            if (j < S.ncand_in[r] && ((cand[idx] >> 8) & 255u) == b2) atomicAdd(&S.hist[1][cand[idx] & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            uint32_t b3, r3;
-            boundary_bin(S.hist[1], remaining, b3, r3);
-            if (tid == 0) {
-                S.res[2] = b3;
-                S.res[3] = r3;
-            }
-        }
-        __syncthreads();
-        remaining = S.res[3];
-        T = prefix | (b2 << 8) | S.res[2];
-        // per CTA: its candidates above the K-th key and equal to it
-        for (uint32_t r = (uint32_t)warp; r < C; r += kThreads / 32) {
-            uint32_t cg = 0, ce = 0;
-            for (uint32_t j = (uint32_t)lane; j < S.ncand_in[r]; j += 32) {
-                const uint32_t key = cand[r * kCandCap + j];
-                cg += key > T ? 1u : 0u;
-                ce += key == T ? 1u : 0u;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                cg += __shfl_xor_sync(0xFFFFFFFFu, cg, off);
-                ce += __shfl_xor_sync(0xFFFFFFFFu, ce, off);
-            }
-            if (lane == 0) {
-                S.gt[r] += cg;
-                S.ecnt[r] = ce;
-            }
-        }
-    } else {
-        exchange_pass(keys, n, prefix, 8, sbuf + C * 256, rank, C, remaining, bstar, S);
-        prefix |= bstar << 8;
-        exchange_pass(keys, n, prefix, 0, sbuf, rank, C, remaining, bstar, S);
-        T = prefix | bstar;
-        if (tid < (int)C) S.ecnt[tid] = sbuf[tid * 256 + bstar];
-    }
-    __syncthreads();  // the per-CTA counts (gt, ecnt) are complete
-    if (tid == 0) {
-        uint32_t ties_before = 0, running = 0;
-        for (uint32_t r = 0; r < C; ++r) {
-            const uint32_t need = remaining > ties_before ? remaining - ties_before : 0u;
-            const uint32_t take = need < S.ecnt[r] ? need : S.ecnt[r];
-            if (r == rank) {
-                S.take_me = take;
-                S.off_me = running;
-            }
-            ties_before += S.ecnt[r];
-            running += S.gt[r] + take;
-        }
-    }
-    __syncthreads();
-    const uint32_t take_me = S.take_me, off_me = S.off_me;
-    // Ordered compaction.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of the local keys: one
-    // pass counts its keys above T and its ties, a block barrier turns the counts into per-warp offsets,
-    // a second pass writes the selected positions in order.  Both passes load four groups of 32 keys
-    // before using them, so the shared-memory latency is not paid once per group.
-    const int nw = kThreads / 32;
-    const int seg = ((n + nw - 1) / nw + 127) / 128 * 128;
-    const int lo = warp * seg, hi = min(n, lo + seg);
-    uint32_t cnt_gt = 0, cnt_tie = 0;
-    for (int base = lo; base < hi; base += 128) {
-        uint32_t k4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * 32 + lane;
-            k4[u] = i < hi ? keys[i] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const bool in = base + u * 32 + lane < hi;
-            cnt_gt += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, in && k4[u] > T));
-            cnt_tie += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, in && k4[u] == T));
-        }
-    }
-    if (lane == 0) {
-        S.scan_e[warp] = cnt_tie;
-        S.scan_s[warp] = cnt_gt;
-    }
-    __syncthreads();
-    uint32_t tie_base = 0, out_base = off_me;
-    for (int k = 0; k < warp; ++k) {
-        const uint32_t ties_k = S.scan_e[k];
-        const uint32_t take_k = take_me > tie_base ? min(ties_k, take_me - tie_base) : 0u;
-        out_base += S.scan_s[k] + take_k;
-        tie_base += ties_k;
-    }
-    if (cnt_gt == 0 && (cnt_tie == 0 || tie_base >= take_me)) return;  // nothing selected in this segment
-    uint32_t run_tie = tie_base, run_sel = 0;
-    for (int base = lo; base < hi; base += 128) {
-        uint32_t k4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * 32 + lane;
-            k4[u] = i < hi ? keys[i] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * 32 + lane;
-            const bool in = i < hi;
-            const bool e = in && k4[u] == T, gsel = in && k4[u] > T;
-            const uint32_t be = __ballot_sync(0xFFFFFFFFu, e);
-            const uint32_t tie_rank = run_tie + (uint32_t)__popc(be & lanemask_lt());
-            const bool sel = gsel || (e && tie_rank < take_me);
-            const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
-            if (sel) out_row[out_base + run_sel + (uint32_t)__popc(bs & lanemask_lt())] = range_start + i;
-            run_tie += (uint32_t)__popc(be);
-            run_sel += (uint32_t)__popc(bs);
-        }
-    }
-}
 
 template <int HI, int DI, int QB, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                         const IndexerParams p) {
-    using Cfg = IdxCfg<HI, DI, QB, FP8>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled operand tiles, by pointer arithmetic on the shared array (an
-    // integer round trip would hide from the compiler that the derived pointers are shared, turning every
-    // access into a slower generic one)
-    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int S = p.stages;
-    uint8_t* a_tiles = smem;                                   // S * kStageBytes
-    uint8_t* q_tile = a_tiles + (size_t)S * Cfg::kStageBytes;  // kQBytes
-    uint32_t* keys = reinterpret_cast<uint32_t*>(q_tile + Cfg::kQBytes);  // QB * chunk
-    float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
-    int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64, padded to 16 bytes
-    // everything after the page list is read with 16-byte vector loads: keep it 16-byte aligned
-    uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + page_words(p.chunk));  // QB x 256
-    uint32_t* allh = hist0 + QB * 256;                                      // C x 768 (select exchange)
-    SelectSmem* sel = reinterpret_cast<SelectSmem*>(allh + 3 * cluster_nctarank() * 256);
-    uint8_t* ctl_raw = reinterpret_cast<uint8_t*>(sel + 1);
-    CtrlSmem* ctl = reinterpret_cast<CtrlSmem*>(ctl_raw + ((16u - (smem_u32(ctl_raw) & 15u)) & 15u));
-
-    // the attention kernel queued behind this one may be scheduled now: it waits on the device before it
-    // reads the Top-K this kernel writes
-    allow_dependent_launch();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t C = cluster_nctarank();
-    const uint32_t rank = cluster_ctarank();
-    const int item = blockIdx.x / (int)C;
-    const int b = item / p.blocks_per_seq;
-    const int jb = item % p.blocks_per_seq;
-    if (b >= p.batch) return;  // uniform over the cluster
-    const int cu0 = p.cu_q_lens[b];
-    const int n_b = p.cu_q_lens[b + 1] - cu0;
-    const int j0 = jb * p.qb;
-    const int L = p.seq_lens[b];
-    if (cu0 < 0 || n_b < 0 || cu0 + n_b > p.total_q) {
-        if (jb == 0 && rank == 0 && tid == 0) raise_error(p.err, DSA_DEVERR_SEQ);
-        return;
-    }
-    if (j0 >= n_b) return;  // uniform over the cluster
-    if (n_b > L || L > p.max_pages * kPage || L < 0) {
-        if (rank == 0 && tid == 0) raise_error(p.err, DSA_DEVERR_SEQ);
-        return;
-    }
-    const int nq = min(p.qb, n_b - j0);
-    const int t0 = cu0 + j0;
-    const int64_t p_last = (int64_t)L - n_b + j0 + nq - 1;  // position of the block's last query
-    const int range_start = (int)rank * p.chunk;
-    const int64_t range_end = (int64_t)range_start + p.chunk;
-    const int64_t hi = range_end < p_last + 1 ? range_end : p_last + 1;
-    const int n_pos = hi > range_start ? (int)(hi - range_start) : 0;
-    const int ntiles = (n_pos + kTileM - 1) / kTileM;
-    const int n_keys = ntiles * kTileM;
-
-    // ---- set-up: page list, head weights, barriers, tensor memory --------------------------------------
-    const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
-    for (int i = tid; i < ntiles * 2; i += kThreads) {
-        const int lp = range_start / kPage + i;
-        int32_t pg = -1;
-        if ((int64_t)lp * kPage < hi) {
-            pg = pt_row[lp];
-            if (pg < 0 || pg >= p.num_pages) {
-                raise_error(p.err, DSA_DEVERR_PAGE);
-                pg = -1;
-            }
-        }
-        pages_s[i] = pg;
-    }
-    for (int i = tid; i < QB * 256; i += kThreads) hist0[i] = 0;
-    for (int c = tid; c < Cfg::kN; c += kThreads) {
-        float wv = 0.f;
-        if (c < nq * HI) {
-            const int64_t idx = (int64_t)(t0 + c / HI) * HI + (c % HI);
-            wv = p.w[idx];
-            if (FP8) wv *= p.q_scale[idx];
-        }
-        w_s[c] = wv;
-    }
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 1);
-        }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&ctl->tfull[i], 1);
-            mbar_init(&ctl->tempty[i], 4);
-        }
-        mbar_init(&ctl->qbar, 1);
-        ctl->consumed = 0;
-        ctl->issued = 0;
-        ctl->qwaited = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1 && ntiles > 0) {
-        tmem_alloc(&ctl->tmem_base, Cfg::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- scoring pipeline -----------------------------------------------------------------------------
-    if (ntiles > 0) {
-        // The producer and MMA warps run their loops with all 32 lanes (every lane waits on the barriers,
-        // one lane issues), so no lane of these warps sits at the block barrier while the loop runs.
-        if (warp == 0) {
-            if (lane == 0) {
-                prefetch_tensormap(&kmap);
-                prefetch_tensormap(&qmap);
-                mbar_arrive_expect_tx(&ctl->qbar, Cfg::kQBytes);
-#pragma unroll
-                for (int a = 0; a < Cfg::kAtoms; ++a)
-                    tma_load_2d(q_tile + a * Cfg::kN * 128, &qmap, &ctl->qbar, a * (128 / Cfg::kElem), t0 * HI);
-            }
-            int issued = 0;
-            int s = 0;  // ring slot and its phase, advanced without a division by the runtime depth
-            uint32_t ph = 0;
-            for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->empty[s], ph ^ 1u, p.err))) break;
-                if (lane == 0) {
-                    const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
-                    const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * (kPage * Cfg::kRowBytes);
-                    if (bytes == 0) {
-                        mbar_arrive(&ctl->full[s]);
-                    } else {
-                        mbar_arrive_expect_tx(&ctl->full[s], bytes);
-                        uint8_t* dst = a_tiles + (size_t)s * Cfg::kStageBytes;
-#pragma unroll
-                        for (int a = 0; a < Cfg::kAtoms; ++a) {
-                            if (pg0 >= 0)
-                                tma_load_3d(dst + a * (kTileM * 128), &kmap, &ctl->full[s], a * (128 / Cfg::kElem),
-                                            0, pg0);
-                            if (pg1 >= 0)
-                                tma_load_3d(dst + a * (kTileM * 128) + kPage * 128, &kmap, &ctl->full[s],
-                                            a * (128 / Cfg::kElem), 0, pg1);
-                        }
-                    }
-                }
-                __syncwarp();
-                issued = i + 1;
-            }
-            if (lane == 0) ctl->issued = issued;
-        } else if (warp == 1) {
-            const uint32_t tmem = ctl->tmem_base;
-            const uint32_t q_base = smem_u32(q_tile);
-            int consumed = 0;
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err));
-            if (lane == 0) ctl->qwaited = ok ? 1 : 0;
-            int s = 0;
-            uint32_t ph = 0;
-            for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-                const int ab = i % Cfg::kAccBufs;
-                const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err))) break;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->full[s], ph, p.err))) break;
-                consumed = i + 1;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_base = smem_u32(a_tiles + (size_t)s * Cfg::kStageBytes);
-#pragma unroll
-                    for (int k = 0; k < Cfg::kKSteps; ++k) {
-                        const int kb = k * Cfg::kMmaK * Cfg::kElem;  // byte offset along K
-                        const int atom = kb / 128, off = kb % 128;
-                        const uint64_t ad = smem_desc(a_base + atom * (kTileM * 128) + off, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(q_base + atom * (Cfg::kN * 128) + off, 16, 1024, kSwizzle128B);
-                        if (FP8)
-                            umma_f8_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
-                        else
-                            umma_f16_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
-                    }
-                    umma_commit(&ctl->empty[s]);
-                    umma_commit(&ctl->tfull[ab]);
-                }
-                __syncwarp();
-            }
-            if (lane == 0) ctl->consumed = consumed;
-        } else if (warp >= 2 && warp < 6) {
-            const uint32_t quad = (uint32_t)(warp & 3);  // TMEM lanes this warp may access
-            const int row = (int)quad * 32 + lane;       // position within the tile
-            const uint32_t tmem = ctl->tmem_base + ((quad * 32u) << 16);
-            int64_t pq[QB];
-#pragma unroll
-            for (int q = 0; q < QB; ++q) pq[q] = (int64_t)L - n_b + j0 + q;
-            for (int i = 0; i < ntiles; ++i) {
-                const int ab = i % Cfg::kAccBufs;
-                const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
-                const int local = i * kTileM + row;
-                const int pos = range_start + local;
-                const int32_t pg = pages_s[2 * i + (row >> 6)];
-                float ksc = 1.f;
-                if (FP8 && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err))) break;
-                tc_fence_after();
-                float acc[QB];
-#pragma unroll
-                for (int q = 0; q < QB; ++q) acc[q] = 0.f;
-                if constexpr (HI % 32 == 0) {
-                    // One query's heads, 32 columns per TMEM wait, in a rolled loop: the code stays small
-                    // (it shares the instruction cache with the MMA warp), eight independent partial sums
-                    // keep the FMA chains short, and the weights come four at a time.
-#pragma unroll
-                    for (int q = 0; q < QB; ++q) {
-                        float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                        for (int c0 = q * HI; c0 < (q + 1) * HI; c0 += 32) {
-                            float v0[16], v1[16];
-                            tmem_ld16(tmem + ab * Cfg::kN + c0, v0);
-                            tmem_ld16(tmem + ab * Cfg::kN + c0 + 16, v1);
-                            tmem_ld_wait();
-                            tmem_regs_ready(v0);
-                            tmem_regs_ready(v1);
-                            const float4* w4 = reinterpret_cast<const float4*>(w_s + c0);
-#pragma unroll
-                            for (int j4 = 0; j4 < 8; ++j4) {
-                                const float4 wv = w4[j4];
-                                const float* v = j4 < 4 ? v0 + 4 * j4 : v1 + 4 * (j4 - 4);
-                                part[(2 * j4) & 7] = fmaf(wv.x, fmaxf(v[0], 0.f), part[(2 * j4) & 7]);
-                                part[(2 * j4 + 1) & 7] = fmaf(wv.y, fmaxf(v[1], 0.f), part[(2 * j4 + 1) & 7]);
-                                part[(2 * j4) & 7] = fmaf(wv.z, fmaxf(v[2], 0.f), part[(2 * j4) & 7]);
-                                part[(2 * j4 + 1) & 7] = fmaf(wv.w, fmaxf(v[3], 0.f), part[(2 * j4 + 1) & 7]);
-                            }
-                        }
-                        acc[q] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                    }
-                } else
-#pragma unroll
-                for (int c0 = 0; c0 < Cfg::kNReal; c0 += 32) {
-                    float v0[16], v1[16];
-                    tmem_ld16(tmem + ab * Cfg::kN + c0, v0);
-                    if (c0 + 16 < Cfg::kNReal) tmem_ld16(tmem + ab * Cfg::kN + c0 + 16, v1);
-                    tmem_ld_wait();
-                    tmem_regs_ready(v0);
-                    if (c0 + 16 < Cfg::kNReal) tmem_regs_ready(v1);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int c = c0 + j;
-                        if (c < Cfg::kNReal) acc[c / HI] += w_s[c] * fmaxf(v0[j], 0.f);
-                    }
-                    if (c0 + 16 < Cfg::kNReal) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int c = c0 + 16 + j;
-                            if (c < Cfg::kNReal) acc[c / HI] += w_s[c] * fmaxf(v1[j], 0.f);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->tempty[ab]);
-#pragma unroll
-                for (int q = 0; q < QB; ++q) {
-                    uint32_t key = 0;
-                    if (q < nq && pg >= 0 && (int64_t)pos <= pq[q]) key = score_key(FP8 ? acc[q] * ksc : acc[q]);
-                    keys[q * p.chunk + local] = key;
-                    // top-byte histogram for the first radix pass (warp-aggregated)
-                    const uint32_t bin = key >> 24;
-                    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&hist0[q * 256 + bin], (uint32_t)__popc(peers));
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (ntiles > 0) {
-        // Drain: copies that were issued but never consumed (only after a timeout) must land before exit.
-        if (warp == 0 && lane == 0) {
-            if (!ctl->qwaited) mbar_wait(&ctl->qbar, 0, p.err);
-            for (int i = ctl->consumed; i < ctl->issued; ++i) mbar_wait(&ctl->full[i % S], (uint32_t)(i / S) & 1u, p.err);
-        }
-        if (warp == 1) tmem_dealloc(ctl->tmem_base, Cfg::kTmemCols);
-    }
-
-    // ---- cluster-wide Top-K per query -------------------------------------------------------------------
-    for (int q = 0; q < nq; ++q) {
-        const int64_t visible = (int64_t)L - n_b + j0 + q + 1;
-        // the smem stage ring is idle once every CTA has scored: it holds the select's fallback exchange space
-        cluster_select(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, reinterpret_cast<uint32_t*>(a_tiles),
-                       n_keys, p.top_k, visible,
-                       p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel);
-    }
-    // No cluster barrier here: every remote access is a histogram push, and the pushes of a pass complete
-    // before that pass's barrier, so after the last pass no CTA touches another's shared memory.
-}
-
-template <int HI, int DI, int QB, bool FP8>
-size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
-    using Cfg = IdxCfg<HI, DI, QB, FP8>;
-    return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
-           (size_t)page_words(chunk) * 4 + (size_t)(QB + 3 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
-           64;
+    indexer_cta<HI, DI, QB, FP8, kThreads, true>(kmap, qmap, p, smem_raw);
 }
 
 template <int HI, int DI, int QB, bool FP8>

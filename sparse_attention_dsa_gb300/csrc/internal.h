@@ -84,6 +84,18 @@ struct SfaLaunch {
 
 cudaError_t launch_sfa(const SfaLaunch& launch, cudaStream_t stream);
 
+// Position splits the attention launcher starts from for these sizes on `num_sms` SMs (before its
+// co-residency check), and the most entries one split may hold.
+int sfa_splits(int64_t total_q, int32_t top_k, int num_sms);
+constexpr int kSfaMaxEntries = 2048;
+
+// Single-launch decode (indexer + Top-K + attention of each token in one cluster, one kernel).  Returns
+// cudaErrorNotSupported, without launching anything, when the sizes do not map one query token to one
+// cluster (the caller then launches the two kernels).
+cudaError_t launch_decode(const IndexerLaunch& indexer, const SfaLaunch& attention, cudaStream_t stream);
+// Whether launch_decode would launch for these plans (no launch).
+bool decode_single_launch(const IndexerLaunch& indexer, const SfaLaunch& attention);
+
 // Split-merge scratch of the attention kernel: each CTA of a grid with position splits owns one region
 // of kSfaMergeRows partial O rows (256 fp32 each; P * ceil(128 / P) of them are used) and 128
 // (max, sum) pairs.

@@ -49,6 +49,18 @@ def _dims(**kw):
 def test_workspace_size(L):
     assert dsa.workspace_size(_dims()) >= 256
     assert L.dsa_workspace_size(None) == 0
+    # few query tokens and K = 2048: the attention may split positions and needs merge scratch
+    # (137 KiB per CTA of the largest grid it may use)
+    ws = dsa.workspace_size(_dims(top_k=2048))
+    assert ws > 256 and (ws - 256) % (136 * 256 * 4 + 256 * 4) == 0
+    # one 64-row tile per query (K = 16), or many query tokens: no splits, just the error word area
+    assert dsa.workspace_size(_dims(top_k=16)) == 256
+    assert dsa.workspace_size(_dims(batch=4096, total_q=4096, top_k=2048)) == 256
+
+
+def test_fused_decode_launches_host_cases(L):
+    assert L.dsa_fused_decode_launches(None) == -1
+    assert dsa.fused_decode_launches(_dims(batch=2, total_q=0)) == 0
 
 
 FAKE = 0x10000  # an aligned non-null value; validation rejects the call before it is ever dereferenced

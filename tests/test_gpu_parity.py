@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import oracle
+import sparse_attention_dsa_gb300 as dsa
 from gen import bf16_to_f32, f32_to_bf16
 from gen.workloads import config, make_workload
 
@@ -158,6 +159,35 @@ def test_topk_scale_jump_across_the_context():
     check_topk(wl, topk)
     out, lse = dw.out_host()
     check_attention(wl, topk, out, lse)
+
+
+def test_fused_decode_launch_count():
+    """One query token per sequence with 64 x 128 indexer heads: one kernel per step; other shapes: two."""
+    assert dsa.fused_decode_launches(DeviceWorkload(_small("hi64_bf16")).dims) == 1
+    assert dsa.fused_decode_launches(DeviceWorkload(config(2, with_sfa=False)).dims) == 1
+    assert dsa.fused_decode_launches(DeviceWorkload(_small("hi64_bf16_two_queries")).dims) == 2
+    assert dsa.fused_decode_launches(DeviceWorkload(_small("hi4_ragged")).dims) == 2
+
+
+@pytest.mark.parametrize("name", ["hi64_bf16", "hi64_fp8", "hi64_salient", "k_equals_one"])
+def test_single_launch_matches_two_kernels(name):
+    """The single-launch kernel selects exactly what the standalone indexer selects, and its attention
+    agrees with the standalone attention kernel's (their position splits may differ, so the fp32
+    summation order may too)."""
+    wl = _small(name) if name != "hi64_fp8" else make_workload("fp8_single", 78, [5000, 190, 700], [1, 1, 1],
+                                                              idx_heads=64, idx_dim=128, idx_fp8=True, top_k=256,
+                                                              attn_heads=128)
+    a = DeviceWorkload(wl)
+    assert dsa.fused_decode_launches(a.dims) == 1
+    a.fused()
+    b = DeviceWorkload(wl).indexer().sfa()
+    assert a.error_word() == 0 and b.error_word() == 0
+    assert np.array_equal(a.topk_host(), b.topk_host())
+    oa, la = a.out_host()
+    ob, lb = b.out_host()
+    np.testing.assert_allclose(oa.astype(np.float32), ob.astype(np.float32), rtol=1e-2, atol=1e-2)
+    np.testing.assert_allclose(la, lb, rtol=1e-5, atol=1e-5)
+    check_attention(wl, a.topk_host(), oa, la)
 
 
 def test_page_permutation_gives_identical_results():
