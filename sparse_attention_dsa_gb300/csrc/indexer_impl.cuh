@@ -598,6 +598,9 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     tma_load_2d(q_tile + a * Cfg::kN * 128, &qmap, &ctl->qbar, a * (128 / Cfg::kElem), t0 * HI);
             }
             int issued = 0;
+            // the K cache is read once per step: evict-first, so its stream does not push the kernel's code
+            // and later inputs out of L2
+            const uint64_t kpol = l2_policy_evict_first();
             int s = 0;  // ring slot and its phase, advanced without a division by the runtime depth
             uint32_t ph = 0;
             for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
@@ -613,11 +616,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
 #pragma unroll
                         for (int a = 0; a < Cfg::kAtoms; ++a) {
                             if (pg0 >= 0)
-                                tma_load_3d(dst + a * (kTileM * 128), &kmap, &ctl->full[s], a * (128 / Cfg::kElem),
-                                            0, pg0);
+                                tma_load_3d_hint(dst + a * (kTileM * 128), &kmap, &ctl->full[s],
+                                                 a * (128 / Cfg::kElem), 0, pg0, kpol);
                             if (pg1 >= 0)
-                                tma_load_3d(dst + a * (kTileM * 128) + kPage * 128, &kmap, &ctl->full[s],
-                                            a * (128 / Cfg::kElem), 0, pg1);
+                                tma_load_3d_hint(dst + a * (kTileM * 128) + kPage * 128, &kmap, &ctl->full[s],
+                                                 a * (128 / Cfg::kElem), 0, pg1, kpol);
                         }
                     }
                 }
