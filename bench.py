@@ -2,9 +2,12 @@
 """Benchmark of the fused DSA decode step on one or more GB300s.
 
 One step = the whole hot path over one batch through dsa_fused_decode: the lightning indexer with
-on-chip Top-K followed by sparse flash attention over the selected rows (the attention kernel is
-launched as a programmatic dependent of the indexer).  Per-kernel durations for the roofline come
-from a second pass of separate dsa_indexer_topk / dsa_sparse_attn calls.  Default workload: decode, 32 sequences x 32768 cached tokens,
+on-chip Top-K followed by sparse flash attention over the selected rows.  At the default workload that
+is one kernel launch (each token's indexer, Top-K and attention run in one thread-block cluster); shapes
+the single-launch kernel does not serve take two launches (the attention kernel as a programmatic
+dependent of the indexer).  The roofline is taken on the dominant launch, timed with CUDA events around
+each launch in a second pass; a third pass times the separate dsa_indexer_topk / dsa_sparse_attn calls
+for the per-kernel breakdown.  Default workload: decode, 32 sequences x 32768 cached tokens,
 one query token each, indexer 64 heads x 128-d bf16, K = 2048, SFA 128 heads x 576-d bf16 (synthetic,
 seeded; inputs larger than L2 so no flush is needed between steps).
 
@@ -199,14 +202,29 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_traffic(kernel_file: str, profile_md: str):
-    """dram bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+# the source files each kernel is built from (a profile is valid only for the sources it was taken on)
+KERNEL_SOURCES = {
+    "indexer": ["indexer.cu", "indexer_impl.cuh", "common.cuh", "internal.h"],
+    "sfa": ["sfa.cu", "sfa_impl.cuh", "common.cuh", "internal.h"],
+    "decode": ["decode.cu", "indexer_impl.cuh", "sfa_impl.cuh", "common.cuh", "internal.h"],
+}
+
+
+def source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sparse_attention_dsa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(kernel: str, profile_md: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the current kernel sources."""
     try:
-        src = open(os.path.join(ROOT, "sparse_attention_dsa_gb300", "csrc", kernel_file), "rb").read()
+        sha = source_sha(kernel)
         txt = open(os.path.join(ROOT, "profiles", profile_md)).read()
     except OSError:
         return None
-    sha = hashlib.sha256(src).hexdigest()[:16]
     m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if not m_sha or not m_b or m_sha.group(1) != sha:
@@ -347,7 +365,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_host1 = time.time()
     barrier(dist)
-    # per-kernel durations (for the roofline): the same work as separate calls with events between them
+    # launch durations for the roofline: the same steps with an event pair around each one
+    launches_per_step = dsa.fused_decode_launches(d)
+    ev_step = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        ev_step[i][0].record(stream)
+        step()
+        ev_step[i][1].record(stream)
+    # per-kernel breakdown: the same work as separate calls with events between them
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     for i in range(K):
         ev[i][0].record(stream)
@@ -358,6 +383,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     sampler.stop()
     total_ms = start.elapsed_time(end)
+    step_ms = sum(e[0].elapsed_time(e[1]) for e in ev_step) / K
     idx_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     sfa_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     if dsa.get_device_error(ws, stream) != 0:
@@ -440,12 +466,15 @@ def run_ours(args):
     topk_host = topk.cpu().numpy()
     b_idx, b_sfa = indexer_bytes(wl), sfa_bytes(wl, topk_host)
     hbm_peak, _, peak_kind = measured_peaks()
-    dominant = "indexer" if idx_ms >= sfa_ms else "sfa"
-    alg = b_idx if dominant == "indexer" else b_sfa
-    dur_ms = idx_ms if dominant == "indexer" else sfa_ms
+    if launches_per_step == 1:
+        # the single-launch kernel carries the whole step
+        dominant, alg, dur_ms = "decode", b_idx + b_sfa, step_ms
+    else:
+        dominant = "indexer" if idx_ms >= sfa_ms else "sfa"
+        alg = b_idx if dominant == "indexer" else b_sfa
+        dur_ms = idx_ms if dominant == "indexer" else sfa_ms
     achieved = alg / (dur_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("indexer.cu" if dominant == "indexer" else "sfa.cu",
-                             f"{dominant}_{CONFIG_NAMES[args.config]}.md")
+    traffic = kernel_traffic(dominant, f"{dominant}_{CONFIG_NAMES[args.config]}.md")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "traffic": traffic, "kernel": dominant, "algorithmic_bytes": alg,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
@@ -461,9 +490,11 @@ def run_ours(args):
                    "query_tokens_per_gpu": T, "top_k": wl.top_k, "idx_heads": wl.idx_heads, "idx_dim": wl.idx_dim,
                    "attn_heads": wl.attn_heads, "kv_dim": wl.kv_dim, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (indexer K cache and latent-KV cache exceed 129 MB); no flush"},
-        "kernel_ms": {"indexer": idx_ms, "sparse_attn": sfa_ms},
+        "kernel_ms": {"step_launch" if launches_per_step == 1 else "step": step_ms,
+                      "indexer_separate": idx_ms, "sparse_attn_separate": sfa_ms},
+        "launches_per_step": launches_per_step,
         "step_bytes": step_bytes, "step_hbm_frac": step_bytes / (t_max_s / K) / 1e9 / hbm_peak,
-        "roofline": roofline, "gpu_launches": 2 * K,
+        "roofline": roofline, "gpu_launches": launches_per_step * K,
         "clocks": sampler.summary(t_host0, t_host1),
     }
     if e2e is not None:

@@ -36,7 +36,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;  // threads of the standalone indexer kernel
+constexpr int kThreads = 384;  // threads of the standalone indexer kernel (warps 6-11 join the select)
 constexpr int kMaxWarps = 16;  // select scratch sized for up to 512 threads
 constexpr int kTileM = 128;  // positions per tile (two pages)
 constexpr int kPage = 64;
@@ -66,6 +66,7 @@ struct IdxCfg {
 };
 
 constexpr int kCandCap = 256;  // second-round candidates one CTA may send (a power of two)
+constexpr int kRankPick = 256;  // up to this many candidates, the K-th key is found by ranking them directly
 
 // Words of the per-CTA page list: one per 64-position page, rounded up to whole 16-byte units.
 __host__ __device__ constexpr int page_words(int chunk) { return ((chunk / kPage) + 3) & ~3; }
@@ -78,11 +79,13 @@ struct SelectSmem {
     uint32_t ecnt[kMaxCluster];      // keys equal to the K-th key, per CTA
     uint32_t guess_in[kMaxCluster];  // round A: every CTA's guess of the top byte (pushed by that CTA)
     uint32_t ncand_in[kMaxCluster];  // round B: every CTA's candidate count (pushed by that CTA)
+    uint32_t sure_in[kMaxCluster];   // round B: every CTA's keys above the 16-bit prefix (pushed by that CTA)
     uint32_t scan_e[kMaxWarps];
     uint32_t scan_s[kMaxWarps];
     uint32_t ncand;
     uint32_t take_me;
     uint32_t off_me;
+    uint8_t cwarp[kCandCap];  // round B: the warp segment each of this CTA's candidates came from
 };
 
 struct CtrlSmem {
@@ -289,12 +292,10 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     bstar = S.res[0];
     remaining = S.res[1];
     const bool spec = S.res[2] != 0;
-    add_above<NT>(ahA, 512, bstar, C, S);
     prefix = bstar << 24;
     if (spec) {
         bstar = S.res[3];
         remaining = S.res[4];
-        add_above<NT>(ahA + 256, 512, bstar, C, S);
         __syncthreads();  // S.res is reused
     } else {
         __syncthreads();
@@ -303,44 +304,101 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     prefix |= bstar << 16;
 
     // ---- round B: the keys that still match the 16-bit prefix, sent to every CTA ----
+    // Warp w scans the contiguous segment [w*seg, (w+1)*seg) of the local keys (the segments of the ordered
+    // compaction below), four keys per lane.  It counts the keys whose top 16 bits exceed the prefix (they
+    // are selected whatever the K-th key turns out to be) and sends every key that matches the prefix to
+    // every CTA, noting which warp's segment it came from.
+    const int nw = NT / 32;
+    const int seg = ((n + nw - 1) / nw + 127) / 128 * 128;
+    const int lo = min(n, warp * seg), hi = min(n, lo + seg);
+    const uint32_t p16 = prefix >> 16;
     if (tid == 0) S.ncand = 0;
+    if (tid < kMaxWarps) S.scan_e[tid] = 0;
     __syncthreads();
-    for (int i0 = 4 * tid; i0 < n; i0 += 4 * NT * 8) {
-        uint4 k8[8];  // eight 16-byte loads in flight (n is a multiple of 128)
+    {
+        uint32_t sure = 0;
+        for (int b0 = lo; b0 < hi; b0 += 4 * 128) {
+            uint4 k4[4];  // four 16-byte loads in flight (segments are multiples of 128 keys)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 4 * NT;
-            k8[u] = i < n ? *reinterpret_cast<const uint4*>(keys + i) : make_uint4(0, 0, 0, 0);
-        }
-        // matches are rare: mark them in a mask here, send them from a small rolled loop below (one copy of
-        // the sending code instead of 32)
-        uint32_t mask = 0;
+            for (int u = 0; u < 4; ++u) {
+                const int i = b0 + u * 128 + 4 * lane;
+                k4[u] = i < hi ? *reinterpret_cast<const uint4*>(keys + i) : make_uint4(0, 0, 0, 0);
+            }
+            // matches are rare: mark them in a mask here, send them from a small rolled loop below
+            uint32_t mask = 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t kv[4] = {k8[u].x, k8[u].y, k8[u].z, k8[u].w};
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t kv[4] = {k4[u].x, k4[u].y, k4[u].z, k4[u].w};
+                const bool in = b0 + u * 128 + 4 * lane < hi;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (i0 + u * 4 * NT < n && ((kv[e] ^ prefix) & 0xFFFF0000u) == 0) mask |= 1u << (4 * u + e);
-        }
+                for (int e = 0; e < 4; ++e) {
+                    sure += (in && (kv[e] >> 16) > p16) ? 1u : 0u;
+                    if (in && (kv[e] >> 16) == p16) mask |= 1u << (4 * u + e);
+                }
+            }
 #pragma unroll 1
-        while (mask != 0) {
-            const int bit = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const uint32_t key = keys[i0 + (bit >> 2) * 4 * NT + (bit & 3)];
-            const uint32_t j = atomicAdd(&S.ncand, 1u);
-            if (j < (uint32_t)kCandCap) {
-                const uint32_t slot = smem_u32(cand + rank * kCandCap + j);
-                for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), key);
+            while (mask != 0) {
+                const int bit = __ffs(mask) - 1;
+                mask &= mask - 1;
+                const uint32_t key = keys[b0 + (bit >> 2) * 128 + 4 * lane + (bit & 3)];
+                const uint32_t j = atomicAdd(&S.ncand, 1u);
+                if (j < (uint32_t)kCandCap) {
+                    S.cwarp[j] = (uint8_t)warp;
+                    const uint32_t slot = smem_u32(cand + rank * kCandCap + j);
+                    for (uint32_t r = 0; r < C; ++r) st_dsmem_u32(mapa_shared(slot, r), key);
+                }
             }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sure += __shfl_xor_sync(0xFFFFFFFFu, sure, off);
+        if (lane == 0) S.scan_s[warp] = sure;
     }
     __syncthreads();
-    if (tid < (int)C) st_dsmem_u32(mapa_shared(smem_u32(&S.ncand_in[rank]), (uint32_t)tid), S.ncand);
+    if (tid < (int)C) {
+        uint32_t sure_cta = 0;
+        for (int w = 0; w < nw; ++w) sure_cta += S.scan_s[w];
+        st_dsmem_u32(mapa_shared(smem_u32(&S.ncand_in[rank]), (uint32_t)tid), S.ncand);
+        st_dsmem_u32(mapa_shared(smem_u32(&S.sure_in[rank]), (uint32_t)tid), sure_cta);
+    }
     cluster_sync();
     const bool fits = __syncthreads_and(tid >= (int)C || S.ncand_in[tid] <= (uint32_t)kCandCap) != 0;
+    // keys above the K-th key per CTA: the sure ones, plus the candidates (or exchanged bins) above it
+    if (tid < kMaxCluster) {
+        S.gt[tid] = tid < (int)C ? S.sure_in[tid] : 0u;
+        S.ecnt[tid] = 0;
+    }
+    uint32_t n_c = 0;  // candidates of the whole cluster
+    for (uint32_t r = 0; r < C; ++r) n_c += S.ncand_in[r];
     uint32_t T;
-    if (fits) {
-        // every CTA holds the same candidate set: find the remaining-th largest among them locally
+    if (fits && n_c <= (uint32_t)kRankPick) {
+        // Every CTA holds the same few candidates: the remaining-th largest of them is the K-th key.  A
+        // thread per candidate counts the candidates above and equal to its own.
+        __syncthreads();
+        for (uint32_t c = (uint32_t)tid; c < n_c; c += NT) {
+            uint32_t r = 0, j = c;
+            while (j >= S.ncand_in[r]) j -= S.ncand_in[r++];
+            const uint32_t key = cand[r * kCandCap + j];
+            uint32_t above = 0, equal = 0;
+            for (uint32_t r2 = 0; r2 < C; ++r2) {
+                const uint32_t* cr = cand + r2 * kCandCap;
+                const uint32_t m = S.ncand_in[r2];
+#pragma unroll 4
+                for (uint32_t j2 = 0; j2 < m; ++j2) {
+                    const uint32_t k2 = cr[j2];
+                    above += k2 > key ? 1u : 0u;
+                    equal += k2 == key ? 1u : 0u;
+                }
+            }
+            if (above < remaining && remaining <= above + equal) {  // every equal candidate writes the same
+                S.res[0] = key;
+                S.res[1] = remaining - above;
+            }
+        }
+        __syncthreads();
+        T = S.res[0];
+        remaining = S.res[1];  // keys equal to T still to take
+    } else if (fits) {
+        // many candidates: their two low bytes, a histogram at a time
         if (tid < 256) {
             S.hist[0][tid] = 0;
             S.hist[1][tid] = 0;
@@ -378,32 +436,50 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         __syncthreads();
         remaining = S.res[3];
         T = prefix | (b2 << 8) | S.res[2];
-        // per CTA: its candidates above the K-th key and equal to it
-        for (uint32_t r = (uint32_t)warp; r < C; r += NT / 32) {
-            uint32_t cg = 0, ce = 0;
-            for (uint32_t j = (uint32_t)lane; j < S.ncand_in[r]; j += 32) {
-                const uint32_t key = cand[r * kCandCap + j];
-                cg += key > T ? 1u : 0u;
-                ce += key == T ? 1u : 0u;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                cg += __shfl_xor_sync(0xFFFFFFFFu, cg, off);
-                ce += __shfl_xor_sync(0xFFFFFFFFu, ce, off);
-            }
-            if (lane == 0) {
-                S.gt[r] += cg;
-                S.ecnt[r] = ce;
+    }
+    if (fits) {
+        // the candidates above T and equal to it: per CTA, and per warp segment for this CTA's own
+        for (uint32_t c = (uint32_t)tid; c < n_c; c += NT) {
+            uint32_t r = 0, j = c;
+            while (j >= S.ncand_in[r]) j -= S.ncand_in[r++];
+            const uint32_t key = cand[r * kCandCap + j];
+            if (key > T) {
+                atomicAdd(&S.gt[r], 1u);
+                if (r == rank) atomicAdd(&S.scan_s[S.cwarp[j]], 1u);
+            } else if (key == T) {
+                atomicAdd(&S.ecnt[r], 1u);
+                if (r == rank) atomicAdd(&S.scan_e[S.cwarp[j]], 1u);
             }
         }
     } else {
+        // too many candidates: a full exchanged pass for each of the two low bytes, then this CTA's
+        // per-warp counts by a pass over its keys
         exchange_pass<NT>(keys, n, prefix, 8, sbuf + C * 256, rank, C, remaining, bstar, S);
         prefix |= bstar << 8;
         exchange_pass<NT>(keys, n, prefix, 0, sbuf, rank, C, remaining, bstar, S);
         T = prefix | bstar;
         if (tid < (int)C) S.ecnt[tid] = sbuf[tid * 256 + bstar];
+        uint32_t cg = 0, ce = 0;
+        for (int b0 = lo; b0 < hi; b0 += 128) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + b0 + 4 * lane);
+            const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                cg += kv[e] > T ? 1u : 0u;
+                ce += kv[e] == T ? 1u : 0u;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            cg += __shfl_xor_sync(0xFFFFFFFFu, cg, off);
+            ce += __shfl_xor_sync(0xFFFFFFFFu, ce, off);
+        }
+        if (lane == 0) {
+            S.scan_s[warp] = cg;
+            S.scan_e[warp] = ce;
+        }
     }
-    __syncthreads();  // the per-CTA counts (gt, ecnt) are complete
+    __syncthreads();  // the per-CTA counts (gt, ecnt) and the per-warp counts are complete
     if (tid == 0) {
         uint32_t ties_before = 0, running = 0;
         for (uint32_t r = 0; r < C; ++r) {
@@ -419,33 +495,9 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     }
     __syncthreads();
     const uint32_t take_me = S.take_me, off_me = S.off_me;
-    // Ordered compaction.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of the local keys: one
-    // pass counts its keys above T and its ties, a block barrier turns the counts into per-warp offsets,
-    // a second pass writes the selected positions in order.  Both passes load four groups of 32 keys
-    // before using them, so the shared-memory latency is not paid once per group.
-    const int nw = NT / 32;
-    const int seg = ((n + nw - 1) / nw + 127) / 128 * 128;
-    const int lo = warp * seg, hi = min(n, lo + seg);
-    uint32_t cnt_gt = 0, cnt_tie = 0;
-    for (int base = lo; base < hi; base += 128) {
-        uint32_t k4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * 32 + lane;
-            k4[u] = i < hi ? keys[i] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const bool in = base + u * 32 + lane < hi;
-            cnt_gt += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, in && k4[u] > T));
-            cnt_tie += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, in && k4[u] == T));
-        }
-    }
-    if (lane == 0) {
-        S.scan_e[warp] = cnt_tie;
-        S.scan_s[warp] = cnt_gt;
-    }
-    __syncthreads();
+    // Ordered compaction: warp w writes the selected positions of its segment after those of the warps
+    // before it.  Per 128 keys (four per lane), four ballots give each key the number of selected keys
+    // (and ties) in earlier lanes.
     uint32_t tie_base = 0, out_base = off_me;
     for (int k = 0; k < warp; ++k) {
         const uint32_t ties_k = S.scan_e[k];
@@ -453,27 +505,48 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         out_base += S.scan_s[k] + take_k;
         tie_base += ties_k;
     }
-    if (cnt_gt == 0 && (cnt_tie == 0 || tie_base >= take_me)) return;  // nothing selected in this segment
-    uint32_t run_tie = tie_base, run_sel = 0;
-    for (int base = lo; base < hi; base += 128) {
-        uint32_t k4[4];
+    if (S.scan_s[warp] == 0 && (S.scan_e[warp] == 0 || tie_base >= take_me)) return;  // nothing selected here
+    const uint32_t lt = lanemask_lt();
+    uint32_t run_tie = tie_base, run_sel = out_base;
+    for (int b0 = lo; b0 < hi; b0 += 128) {
+        const int i = b0 + 4 * lane;
+        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
+        const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+        uint32_t bt[4], tm = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * 32 + lane;
-            k4[u] = i < hi ? keys[i] : 0u;
+        for (int e = 0; e < 4; ++e) {
+            const bool t = kv[e] == T;
+            bt[e] = __ballot_sync(0xFFFFFFFFu, t);
+            tm |= (t ? 1u : 0u) << e;
+        }
+        uint32_t tie_rank = run_tie;  // ties at earlier positions of this CTA
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tie_rank += (uint32_t)__popc(bt[e] & lt);
+        uint32_t sm = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool t = (tm >> e) & 1u;
+            const bool sel = kv[e] > T || (t && tie_rank < take_me);
+            tie_rank += t ? 1u : 0u;
+            sm |= (sel ? 1u : 0u) << e;
+        }
+        uint32_t bs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bs[e] = __ballot_sync(0xFFFFFFFFu, (sm >> e) & 1u);
+        uint32_t pos = run_sel;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pos += (uint32_t)__popc(bs[e] & lt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if ((sm >> e) & 1u) {
+                if (pos < (uint32_t)K) out_row[pos] = range_start + i + e;
+                ++pos;
+            }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * 32 + lane;
-            const bool in = i < hi;
-            const bool e = in && k4[u] == T, gsel = in && k4[u] > T;
-            const uint32_t be = __ballot_sync(0xFFFFFFFFu, e);
-            const uint32_t tie_rank = run_tie + (uint32_t)__popc(be & lanemask_lt());
-            const bool sel = gsel || (e && tie_rank < take_me);
-            const uint32_t bs = __ballot_sync(0xFFFFFFFFu, sel);
-            if (sel) out_row[out_base + run_sel + (uint32_t)__popc(bs & lanemask_lt())] = range_start + i;
-            run_tie += (uint32_t)__popc(be);
-            run_sel += (uint32_t)__popc(bs);
+        for (int e = 0; e < 4; ++e) {
+            run_tie += (uint32_t)__popc(bt[e]);
+            run_sel += (uint32_t)__popc(bs[e]);
         }
     }
 }
