@@ -25,6 +25,9 @@ Recipe (identical for every config and for the small test cases):
   have their indexer key multiplied by 4 (exact in bf16).
 * FP8 inputs: bf16 values quantised per row (one row = one token's 128-d key, or one (token, head)
   query row) with scale = absmax/448.
+* FP8 latent-KV cache (kv_fp8): the same bf16 rows, each 128-dim tile of the leading Dv dims quantised
+  with its own absmax/448 scale; row layout 656 bytes = Dv codes, Dv/128 fp32 scales, the remaining
+  (rotary) dims as bf16.
 """
 from __future__ import annotations
 
@@ -75,8 +78,9 @@ class Workload:
     v_dim: int
     softmax_scale: float
     q: Optional[np.ndarray] = None  # bf16 bits uint16 [T, Hq, kv_dim]
-    kv_cache: Optional[np.ndarray] = None  # bf16 bits uint16 [P, 64, kv_dim]
+    kv_cache: Optional[np.ndarray] = None  # bf16 bits uint16 [P, 64, kv_dim], or uint8 [P, 64, 656] (kv_fp8)
     notes: dict = field(default_factory=dict)
+    kv_fp8: bool = False
 
     @property
     def batch(self) -> int:
@@ -136,7 +140,7 @@ def make_workload(name: str, seed: int, seq_lens: Sequence[int], q_lens: Sequenc
                   idx_dim: int, idx_fp8: bool, top_k: int, attn_heads: int, kv_dim: int = 576, v_dim: int = 512,
                   w_hi: float = 1.0, salient_frac: float = 0.0, salient_mult: float = 4.0,
                   page_size: int = PAGE_SIZE, softmax_scale: Optional[float] = None, with_sfa: bool = True,
-                  page_seed: Optional[int] = None) -> Workload:
+                  page_seed: Optional[int] = None, kv_fp8: bool = False) -> Workload:
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     q_lens = np.asarray(q_lens, dtype=np.int32)
     assert seq_lens.shape == q_lens.shape
@@ -173,12 +177,34 @@ def make_workload(name: str, seed: int, seq_lens: Sequence[int], q_lens: Sequenc
     if with_sfa:
         q = normal_bf16(stream_key(seed, T_Q), T * attn_heads * kv_dim).reshape(T, attn_heads, kv_dim)
         kv = paged_normal_bf16(stream_key(seed, T_KV), seq_lens, pt, page_size, kv_dim, row_stride_b, num_pages)
+        if kv_fp8:
+            kv = kv_rows_to_fp8(kv, v_dim)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(kv_dim)
     return Workload(name=name, seed=seed, seq_lens=seq_lens, cu_q_lens=cu, page_size=page_size, page_table=pt,
                     num_pages=num_pages, idx_heads=idx_heads, idx_dim=idx_dim, idx_fp8=idx_fp8, q_idx=q_idx,
                     q_scale=q_scale, w=w, k_cache=k_cache, k_scale=k_scale, top_k=top_k, attn_heads=attn_heads,
-                    kv_dim=kv_dim, v_dim=v_dim, softmax_scale=float(softmax_scale), q=q, kv_cache=kv, notes=notes)
+                    kv_dim=kv_dim, v_dim=v_dim, softmax_scale=float(softmax_scale), q=q, kv_cache=kv, notes=notes,
+                    kv_fp8=bool(kv_fp8 and with_sfa))
+
+
+def kv_fp8_row_bytes(kv_dim: int = 576, v_dim: int = 512) -> int:
+    return v_dim + 4 * (v_dim // 128) + 2 * (kv_dim - v_dim)
+
+
+def kv_rows_to_fp8(kv_bf16: np.ndarray, v_dim: int = 512) -> np.ndarray:
+    """bf16-bits rows [..., kv_dim] -> uint8 rows [..., 656] in the FP8 latent-KV layout (input synthesis)."""
+    kv = np.ascontiguousarray(kv_bf16, dtype=np.uint16)
+    lead, kv_dim = kv.shape[:-1], kv.shape[-1]
+    n = int(np.prod(lead)) if lead else 1
+    flat = kv.reshape(n, kv_dim)
+    tiles = np.ascontiguousarray(flat[:, :v_dim]).reshape(n * (v_dim // 128), 128)
+    codes, scales = quantize_e4m3_rows(tiles)
+    out = np.empty((n, kv_fp8_row_bytes(kv_dim, v_dim)), dtype=np.uint8)
+    out[:, :v_dim] = codes.reshape(n, v_dim)
+    out[:, v_dim:v_dim + 4 * (v_dim // 128)] = scales.reshape(n, v_dim // 128).view(np.uint8).reshape(n, -1)
+    out[:, v_dim + 4 * (v_dim // 128):] = np.ascontiguousarray(flat[:, v_dim:]).view(np.uint8).reshape(n, -1)
+    return out.reshape(*lead, out.shape[-1])
 
 
 CONFIG_NAMES = {
@@ -205,13 +231,15 @@ def config_lengths(n: int, seed: Optional[int] = None):
     raise ValueError(n)
 
 
-def config(n: int, seed: Optional[int] = None, with_sfa: bool = True, batch: Optional[int] = None) -> Workload:
-    """Workload of configuration n (1..5).  `batch` truncates to the first sequences (same data)."""
+def config(n: int, seed: Optional[int] = None, with_sfa: bool = True, batch: Optional[int] = None,
+           kv_fp8: bool = False) -> Workload:
+    """Workload of configuration n (1..5).  `batch` truncates to the first sequences (same data);
+    `kv_fp8` stores the latent-KV cache in the FP8 layout (same bf16 rows, quantised)."""
     seed = 1000 + n if seed is None else seed
     lens, qls = config_lengths(n, seed)
     if batch is not None:
         lens, qls = lens[:batch], qls[:batch]
-    common = dict(with_sfa=with_sfa)
+    common = dict(with_sfa=with_sfa, kv_fp8=kv_fp8)
     if n == 1:
         return make_workload(CONFIG_NAMES[1], seed, lens, qls, idx_heads=4, idx_dim=64, idx_fp8=False, top_k=256,
                              attn_heads=16, w_hi=1.0, **common)

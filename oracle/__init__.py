@@ -48,6 +48,7 @@ class _Dims(ctypes.Structure):
         ("attn_heads", ctypes.c_int32),
         ("kv_dim", ctypes.c_int32),
         ("v_dim", ctypes.c_int32),
+        ("kv_fp8", ctypes.c_int32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -80,6 +81,12 @@ def lib():
             L.oracle_index_scores_batch.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 9 + [i32, ctypes.c_int64, vp]
             L.oracle_sparse_attn.restype = ctypes.c_int
             L.oracle_sparse_attn.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 7 + [i32, vp, vp, vp]
+            L.oracle_e4m3_encode.restype = ctypes.c_uint8
+            L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            L.oracle_quantize_group.restype = None
+            L.oracle_quantize_group.argtypes = [vp, i32, vp, vp]
+            L.oracle_append_rows.restype = ctypes.c_int
+            L.oracle_append_rows.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 8
             _lib = L
     return _lib
 
@@ -95,7 +102,7 @@ def _dims(wl) -> _Dims:
     return _Dims(batch=wl.batch, total_q=wl.total_q, num_pages=wl.num_pages, page_size=wl.page_size,
                  max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads, idx_dim=wl.idx_dim,
                  idx_fp8=1 if wl.idx_fp8 else 0, top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim,
-                 v_dim=wl.v_dim, softmax_scale=wl.softmax_scale)
+                 v_dim=wl.v_dim, kv_fp8=1 if getattr(wl, "kv_fp8", False) else 0, softmax_scale=wl.softmax_scale)
 
 
 def _check(rc):
@@ -167,3 +174,35 @@ def sparse_attn(wl, topk, tlist=None, want_weights: bool = False):
                                   _p(wl.seq_lens), _p(wl.cu_q_lens), _p(topk), _p(tl), nt, _p(out), _p(lse), _p(wts))
     _check(rc)
     return (out, lse, wts) if want_weights else (out, lse)
+
+
+def e4m3_encode(y: float) -> int:
+    """E4M3 code of the fp32 value y: nearest finite value, ties to the even code, saturating at 448."""
+    return int(lib().oracle_e4m3_encode(float(y)))
+
+
+def quantize_group(x) -> tuple:
+    """(codes uint8 [n], scale float32) of one quantisation group: scale = absmax/448 (fp32), codes of x/scale."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    codes = np.empty(x.shape[0], dtype=np.uint8)
+    scale = np.empty(1, dtype=np.float32)
+    lib().oracle_quantize_group(_p(x), int(x.shape[0]), _p(codes), _p(scale))
+    return codes, np.float32(scale[0])
+
+
+def append(wl, k_new=None, kv_new=None):
+    """Copies of (k_cache, k_scale, kv_cache) after appending every query token's new rows at its position
+    (k_new: bf16 bits [T, Di] or None; kv_new: bf16 bits [T, kv_dim] or None)."""
+    k_cache = np.array(wl.k_cache, copy=True)
+    k_scale = np.array(wl.k_scale, copy=True) if wl.k_scale is not None else None
+    kv_cache = np.array(wl.kv_cache, copy=True) if wl.kv_cache is not None else None
+    kn = np.ascontiguousarray(k_new, dtype=np.uint16) if k_new is not None else None
+    kvn = np.ascontiguousarray(kv_new, dtype=np.uint16) if kv_new is not None else None
+    if kn is not None:
+        assert kn.shape == (wl.total_q, wl.idx_dim)
+    if kvn is not None:
+        assert kvn.shape == (wl.total_q, wl.kv_dim) and kv_cache is not None
+    rc = lib().oracle_append_rows(ctypes.byref(_dims(wl)), _p(kn), _p(kvn), _p(wl.page_table), _p(wl.seq_lens),
+                                  _p(wl.cu_q_lens), _p(k_cache), _p(k_scale), _p(kv_cache))
+    _check(rc)
+    return k_cache, k_scale, kv_cache

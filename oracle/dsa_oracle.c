@@ -31,6 +31,18 @@
  *  - attention over the selected rows: z = scale * q . kv (all 576 dims), softmax over the selected
  *    set, out = sum softmax * kv[:, :Dv] (V = leading Dv dims of the same latent row),
  *    lse = max z + log sum exp(z - max z) (natural log).  No selected row: out = 0, lse = -inf.
+ *  - FP8 latent-KV cache ([A1] section 1 layered quantization; [A4] section 4 hierarchical quantization:
+ *    FP8 with one scale per 128 elements of each token): the latent part (the leading Dv = 512 dims)
+ *    is 4 tiles of 128 E4M3 codes, each with its own fp32 scale; the remaining 64 rotary dims stay bf16
+ *    (576 is not a multiple of 128).  Row layout, 656 bytes: 512 codes, 4 fp32 scales, 64 bf16 values.
+ *    An element is code value x its tile's scale, applied literally.
+ *  - appending a step's rows ([A4] section 3.3, the K input of the indexer; quantisation as in [A1]
+ *    section 1): query token t's new indexer key and latent-KV row go to the cache row of its own
+ *    position p_t.  FP8 caches quantise dynamically: scale = absmax / 448 over the quantisation group
+ *    (the indexer key row; each 128-element latent tile), 1 when the group is all zero, and
+ *    code = E4M3(x / scale) rounded to nearest, ties to the even code, saturating at 448.  The pages fix
+ *    no precision for this; absmax, scale and x / scale are taken in fp32 (IEEE, correctly rounded),
+ *    the precision of the GPU kernel, so both make the same integer decisions.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,6 +62,7 @@ typedef struct {
     int32_t attn_heads;
     int32_t kv_dim;
     int32_t v_dim;
+    int32_t kv_fp8; /* 0: kv rows are bf16 bits; 1: the 656-byte FP8 layout above */
     double softmax_scale;
 } oracle_dims;
 
@@ -76,6 +89,62 @@ double oracle_e4m3_value(uint8_t code) {
     else
         v = ldexp(1.0 + (double)m / 8.0, e - 7);
     return sign ? -v : v;
+}
+
+/* E4M3 code of y: the nearest of the finite values (codes 0x00..0x7E and their negatives) by scanning
+ * them all, ties to the even code; beyond 448 in magnitude the result is +-448 (saturation); NaN gives
+ * 0x7F.  Zero keeps its sign. */
+uint8_t oracle_e4m3_encode(float y) {
+    if (y != y) return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Dynamic E4M3 quantisation of one group of n values (see the readings at the top):
+ * *scale = absmax / 448 in fp32 (1 for an all-zero group), codes[i] = E4M3(x[i] / *scale) in fp32. */
+void oracle_quantize_group(const float* x, int32_t n, uint8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int32_t i = 0; i < n; ++i)
+        if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+    float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int32_t i = 0; i < n; ++i) {
+        float y = x[i] / s;
+        codes[i] = oracle_e4m3_encode(y);
+    }
+    *scale = s;
+}
+
+/* Bytes of one latent-KV cache row. */
+static int64_t kv_row_bytes(const oracle_dims* d) {
+    if (!d->kv_fp8) return (int64_t)d->kv_dim * 2;
+    return (int64_t)d->v_dim + 4 * (d->v_dim / 128) + 2 * ((int64_t)d->kv_dim - d->v_dim);
+}
+
+/* Element c of latent-KV cache row `row` (either layout). */
+static double kv_elem(const oracle_dims* d, const void* kv_cache, int64_t row, int32_t c) {
+    const uint8_t* r = (const uint8_t*)kv_cache + row * kv_row_bytes(d);
+    uint16_t bits;
+    if (!d->kv_fp8) {
+        memcpy(&bits, r + 2 * (int64_t)c, 2);
+        return oracle_bf16_value(bits);
+    }
+    if (c < d->v_dim) {
+        float scale;
+        memcpy(&scale, r + d->v_dim + 4 * (c / 128), 4);
+        return oracle_e4m3_value(r[c]) * (double)scale;
+    }
+    memcpy(&bits, r + d->v_dim + 4 * (d->v_dim / 128) + 2 * (int64_t)(c - d->v_dim), 2);
+    return oracle_bf16_value(bits);
 }
 
 /* Sequence of query token t and its causal position. */
@@ -249,7 +318,7 @@ int oracle_indexer_topk(const oracle_dims* d, const void* q_idx, const float* q_
  * topk rows are indexed by list position i (row i belongs to token tlist[i]).
  * weights (optional, [nt, H, K]) receives softmax(z) in topk order (0 for -1 entries).
  */
-int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const uint16_t* kv_cache,
+int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const void* kv_cache,
                        const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
                        const int32_t* topk, const int32_t* tlist, int32_t nt, double* out, double* lse,
                        double* weights) {
@@ -302,9 +371,8 @@ int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const uint16_t* 
             int32_t count = 0;
             for (int32_t k = 0; k < K; ++k) {
                 if (rows[k] < 0) continue;
-                const uint16_t* r = kv_cache + rows[k] * C;
                 double dot = 0.0;
-                for (int32_t c = 0; c < C; ++c) dot += oracle_bf16_value(qh[c]) * oracle_bf16_value(r[c]);
+                for (int32_t c = 0; c < C; ++c) dot += oracle_bf16_value(qh[c]) * kv_elem(d, kv_cache, rows[k], c);
                 z[k] = d->softmax_scale * dot;
                 if (z[k] > zmax) zmax = z[k];
                 ++count;
@@ -325,8 +393,7 @@ int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const uint16_t* 
                 if (rows[k] < 0) continue;
                 double a = exp(z[k] - zmax) / denom;
                 if (wrow) wrow[k] = a;
-                const uint16_t* r = kv_cache + rows[k] * C;
-                for (int32_t v = 0; v < V; ++v) o[v] += a * oracle_bf16_value(r[v]);
+                for (int32_t v = 0; v < V; ++v) o[v] += a * kv_elem(d, kv_cache, rows[k], v);
             }
             lse[(int64_t)i * H + h] = zmax + log(denom);
         }
@@ -355,5 +422,57 @@ int oracle_index_scores_batch(const oracle_dims* d, const void* q_idx, const flo
             err = (int)got;
         }
     }
+    return err;
+}
+
+/*
+ * Appending one decode/prefill step's rows to the paged caches (readings at the top): for every query
+ * token t, its new indexer key k_new[t] (bf16 bits [T, Di], or NULL) goes to the indexer cache row of
+ * position p_t (bf16 copy, or E4M3 codes with the row's scale in k_scale), and its new latent-KV row
+ * kv_new[t] (bf16 bits [T, kv_dim], or NULL) to the latent-KV cache row of p_t (bf16 copy, or the FP8
+ * layout).  Returns 0 or the first error code met (nothing is written for a token with an error).
+ */
+int oracle_append_rows(const oracle_dims* d, const uint16_t* k_new, const uint16_t* kv_new, const int32_t* page_table,
+                       const int32_t* seq_lens, const int32_t* cu_q_lens, void* k_cache, float* k_scale,
+                       void* kv_cache) {
+    int err = 0;
+    float* x = (float*)malloc(sizeof(float) * (size_t)(d->idx_dim > d->kv_dim ? d->idx_dim : d->kv_dim));
+    if (!x) return ORC_NOMEM;
+    for (int32_t t = 0; t < d->total_q; ++t) {
+        int32_t b;
+        int64_t p, row;
+        int rc = query_locate(d, seq_lens, cu_q_lens, t, &b, &p);
+        if (!rc) rc = page_row(d, page_table, b, p, &row);
+        if (rc) {
+            if (!err) err = rc;
+            continue;
+        }
+        if (k_new) {
+            const uint16_t* src = k_new + (int64_t)t * d->idx_dim;
+            if (d->idx_fp8) {
+                for (int32_t c = 0; c < d->idx_dim; ++c) x[c] = (float)oracle_bf16_value(src[c]);
+                oracle_quantize_group(x, d->idx_dim, (uint8_t*)k_cache + row * d->idx_dim, &k_scale[row]);
+            } else {
+                memcpy((uint16_t*)k_cache + row * d->idx_dim, src, sizeof(uint16_t) * (size_t)d->idx_dim);
+            }
+        }
+        if (kv_new) {
+            const uint16_t* src = kv_new + (int64_t)t * d->kv_dim;
+            uint8_t* dst = (uint8_t*)kv_cache + row * kv_row_bytes(d);
+            if (d->kv_fp8) {
+                for (int32_t c = 0; c < d->v_dim; ++c) x[c] = (float)oracle_bf16_value(src[c]);
+                for (int32_t tile = 0; tile < d->v_dim / 128; ++tile) {
+                    float scale;
+                    oracle_quantize_group(x + 128 * tile, 128, dst + 128 * tile, &scale);
+                    memcpy(dst + d->v_dim + 4 * tile, &scale, 4);
+                }
+                memcpy(dst + d->v_dim + 4 * (d->v_dim / 128), src + d->v_dim,
+                       sizeof(uint16_t) * (size_t)(d->kv_dim - d->v_dim));
+            } else {
+                memcpy(dst, src, sizeof(uint16_t) * (size_t)d->kv_dim);
+            }
+        }
+    }
+    free(x);
     return err;
 }

@@ -290,3 +290,121 @@ def test_bad_page_is_reported():
     wl.page_table[0, 0] = wl.num_pages + 3
     with pytest.raises(oracle.OracleError):
         oracle.indexer_topk(wl)
+
+
+# ---------------------------------------------------------------------------------------------------
+# FP8 latent-KV cache and appending a step's rows
+# ---------------------------------------------------------------------------------------------------
+
+
+def _torch_e4m3(x):
+    """E4M3 codes of float32 values by torch's float8_e4m3fn conversion (finite range only)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_e4m3_value(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_oracle_e4m3_encoder_round_trips_every_finite_code():
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c, hex(c)
+
+
+def test_oracle_e4m3_encoder_matches_torch_and_ties_to_even():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.uniform(-448, 448, 6000), rng.normal(0, 1, 6000),
+                        rng.uniform(-2.0 ** -5, 2.0 ** -5, 3000)]).astype(np.float32)
+    ours = np.array([oracle.e4m3_encode(v) for v in x], dtype=np.uint8)
+    assert np.array_equal(ours, _torch_e4m3(x))
+    # midpoints between neighbouring finite values go to the even code (torch agrees)
+    vals = _torch_e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    ours = np.array([oracle.e4m3_encode(v) for v in mids])
+    lo = np.arange(0x7E)
+    assert np.array_equal(ours, np.where(lo % 2 == 0, lo, lo + 1))
+    assert np.array_equal(ours, _torch_e4m3(mids))
+    assert oracle.e4m3_encode(449.0) == 0x7E and oracle.e4m3_encode(-1e6) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_quantize_group_is_absmax_over_448_in_fp32():
+    rng = np.random.default_rng(9)
+    for mag in (1e-3, 1.0, 37.0, 3e4):
+        x = (bf16_to_f32((rng.normal(0, 1, 128).astype(np.float32) * np.float32(mag)).view(np.uint32) >> 16)
+             .astype(np.float32))
+        codes, scale = oracle.quantize_group(x)
+        amax = np.float32(np.max(np.abs(x)))
+        assert scale == amax / np.float32(448.0)
+        assert np.array_equal(codes, _torch_e4m3(x / scale))
+        assert codes[np.argmax(np.abs(x))] & 0x7F == 0x7E
+    codes, scale = oracle.quantize_group(np.zeros(128, dtype=np.float32))
+    assert scale == 1.0 and np.all(codes == 0)
+
+
+def _fp8_kv_rows(rng, n, v_dim=512, kv_dim=576):
+    """Random FP8 latent-KV rows built byte by byte (codes, power-of-two tile scales, bf16 rope) and the
+    same rows as exact bf16 values (e4m3 x 2^k has at most four significant bits)."""
+    tiles = v_dim // 128
+    codes = rng.integers(0, 0x7F, (n, v_dim)).astype(np.uint8) | (rng.integers(0, 2, (n, v_dim)) << 7).astype(np.uint8)
+    scales = (2.0 ** rng.integers(-4, 5, (n, tiles))).astype(np.float32)
+    rope_f = rng.normal(0, 1, (n, kv_dim - v_dim)).astype(np.float32)
+    rope = (rope_f.view(np.uint32) >> 16).astype(np.uint16)
+    fp8 = np.empty((n, v_dim + 4 * tiles + 2 * (kv_dim - v_dim)), dtype=np.uint8)
+    fp8[:, :v_dim] = codes
+    fp8[:, v_dim:v_dim + 4 * tiles] = scales.view(np.uint8).reshape(n, 4 * tiles)
+    fp8[:, v_dim + 4 * tiles:] = rope.view(np.uint8).reshape(n, -1)
+    vals = _torch_e4m3_value(codes) * np.repeat(scales.astype(np.float64), 128, axis=1)
+    bf = np.empty((n, kv_dim), dtype=np.uint16)
+    bf[:, :v_dim] = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bf16_to_f32(bf[:, :v_dim]).astype(np.float64), vals)  # exact in bf16
+    bf[:, v_dim:] = rope
+    return fp8, bf
+
+
+def test_fp8_kv_attention_equals_bf16_attention_on_the_same_values():
+    wl = _small(top_k=16, kv_dim=576, v_dim=512, hq=3)
+    rng = np.random.default_rng(21)
+    P = wl.kv_cache.shape[0] * wl.kv_cache.shape[1]
+    fp8, bf = _fp8_kv_rows(rng, P)
+    wl.kv_cache = bf.reshape(wl.kv_cache.shape)
+    topk, _, _ = oracle.indexer_topk(wl)
+    out_bf, lse_bf = oracle.sparse_attn(wl, topk)
+    wl.kv_cache = fp8.reshape(wl.kv_cache.shape[0], wl.kv_cache.shape[1], -1)
+    wl.kv_fp8 = True
+    out_f8, lse_f8 = oracle.sparse_attn(wl, topk)
+    assert np.array_equal(out_f8, out_bf) and np.array_equal(lse_f8, lse_bf)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_append_writes_each_token_row_at_its_position(fp8):
+    wl = _small(idx_fp8=fp8, top_k=16, kv_dim=576, v_dim=512, hq=2, kv_fp8=fp8)
+    rng = np.random.default_rng(33 + fp8)
+    T = wl.total_q
+    k_new = (rng.normal(0, 2, (T, wl.idx_dim)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kv_new = (rng.normal(0, 2, (T, wl.kv_dim)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    k_cache, k_scale, kv_cache = oracle.append(wl, k_new, kv_new)
+    touched = set()
+    for t, p in enumerate(wl.query_positions()):
+        b = int(wl.query_seq()[t])
+        page, slot = int(wl.page_table[b, p // wl.page_size]), int(p % wl.page_size)
+        touched.add((page, slot))
+        if not fp8:
+            assert np.array_equal(k_cache[page, slot], k_new[t]) and np.array_equal(kv_cache[page, slot], kv_new[t])
+            continue
+        x = bf16_to_f32(k_new[t])
+        s = np.float32(np.max(np.abs(x))) / np.float32(448.0)
+        assert k_scale[page, slot] == s and np.array_equal(k_cache[page, slot], _torch_e4m3(x / s))
+        row = kv_cache[page, slot]
+        for tile in range(4):
+            xt = bf16_to_f32(kv_new[t, 128 * tile:128 * (tile + 1)])
+            st = np.float32(np.max(np.abs(xt))) / np.float32(448.0)
+            assert row[512 + 4 * tile:516 + 4 * tile].view(np.float32)[0] == st
+            assert np.array_equal(row[128 * tile:128 * (tile + 1)], _torch_e4m3(xt / st))
+        assert np.array_equal(row[528:].view(np.uint16), kv_new[t, 512:])
+    for page in range(k_cache.shape[0]):
+        for slot in range(k_cache.shape[1]):
+            if (page, slot) in touched:
+                continue
+            assert np.array_equal(k_cache[page, slot], wl.k_cache[page, slot])
+            assert np.array_equal(kv_cache[page, slot], wl.kv_cache[page, slot])
