@@ -5,14 +5,16 @@
  *
  * The operations follow these published articles (cited by title and section):
  *  [A1] "Optimizing Inference for Hybrid Attention LLMs: Practices for Fast Adaptation", sections 1 and
- *       3.2 (index-gather-compute integration; paged KV management; gather/compute overlap).
+ *       3.2 (index-gather-compute integration; paged KV management; gather/compute overlap; layered
+ *       quantization: FP8 KV cache with one scale per 128 elements of each token).
  *  [A2] "Optimizing Inference for Hybrid Attention Architectures: From Operator Fusion to Sequence
  *       Sharding", section "Breaking Down the Computational Path of Hybrid Attention" (steps 1 and 2) and
  *       section "Fusing Index Screening with Multi-Stream Orchestration".
  *  [A3] "Day0 Inference Optimization for Next-Generation Hybrid-Architecture LLMs Based on CANN",
  *       sections 2.1 (deep operator fusion) and 3.1 (FP8 indexer inputs).
  *  [A4] "Day0 Inference Support and Performance Optimization for New LLM Architectures", sections 3.1
- *       (integrated indexer fusion) and 3.2 (sparse attention kernel).
+ *       (integrated indexer fusion), 3.2 (sparse attention kernel), 3.3 (input preparation ahead of the
+ *       indexer) and 4 (hierarchical quantization: "Token-Head-Tile" FP8 KV cache, tiles of 128).
  *
  * Conventions shared by every entry point
  *  - Ownership: the caller owns every buffer.  All array arguments are DEVICE pointers (memory of the
@@ -44,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 typedef enum {
     DSA_OK = 0,
@@ -57,8 +59,19 @@ typedef enum {
 
 typedef enum {
     DSA_BF16 = 0,     /* bfloat16 */
-    DSA_FP8_E4M3 = 1  /* OCP OFP8 E4M3 codes, each row with one fp32 scale ([A3] 3.1) */
+    DSA_FP8_E4M3 = 1  /* OCP OFP8 E4M3 codes times fp32 scales: indexer rows with one scale per row
+                         ([A3] 3.1); latent-KV rows in the FP8 row layout below */
 } dsa_dtype_t;
+
+/*
+ * FP8 latent-KV row layout ([A1] 1 and [A4] 4: FP8 with one scale per 128 elements of each token), used
+ * when dims->kv_dtype == DSA_FP8_E4M3 (D = 576, Dv = 512).  One row is DSA_KV_FP8_ROW_BYTES bytes:
+ *   bytes   0..511  E4M3 codes of dims 0..511 (the latent part, also V), in 4 tiles of 128;
+ *   bytes 512..527  4 fp32 scales, tile i covering dims 128*i .. 128*i+127;
+ *   bytes 528..655  dims 512..575 (the rotary part) as bf16, unquantised (576 is not a multiple of 128).
+ * Element d < 512 of the row is e4m3(code[d]) * scale[d / 128]; the kernels dequantise to bf16.
+ */
+#define DSA_KV_FP8_ROW_BYTES 656
 
 /* Bits of the device error word (the first int32 of the workspace). */
 #define DSA_DEVERR_PAGE 0x1    /* a page-table entry outside [0, num_pages) was needed */
@@ -81,6 +94,8 @@ typedef struct {
     int32_t kv_dim;            /* D, latent KV row width (512 latent + 64 RoPE = 576) */
     int32_t v_dim;             /* Dv, leading dims of each row used as V (512) */
     float softmax_scale;       /* multiplies q . kv before the softmax (1/sqrt(576)) */
+    int32_t kv_dtype;          /* dsa_dtype_t of the latent-KV cache: DSA_BF16 rows of D values, or
+                                  DSA_FP8_E4M3 rows in the FP8 row layout above */
 } dsa_dims_t;
 
 /* ABI version of the loaded library (DSA_ABI_VERSION). */
@@ -134,7 +149,9 @@ dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const f
  *     z_s = softmax_scale * q[t,h,:] . kv[s,:]           (all kv_dim dims)
  *     out[t,h,:] = sum_{s in S_t} softmax(z)_s * kv[s, 0:v_dim]
  *     lse[t,h]   = log sum_{s in S_t} exp(z_s)           (natural log; -inf and out = 0 if S_t is empty)
- *   q          [T, Hq, D] bf16;  kv_cache [num_pages, 64, D] bf16 (V = the first Dv dims of each row)
+ *   q          [T, Hq, D] bf16
+ *   kv_cache   [num_pages, 64, D] bf16, or [num_pages, 64, DSA_KV_FP8_ROW_BYTES] bytes in the FP8 row
+ *              layout when dims->kv_dtype == DSA_FP8_E4M3 (V = the first Dv dims of each row)
  *   topk_idx   [T, K] int32 logical positions (entries outside [-1, p_t] set DSA_DEVERR_INDEX and are
  *              skipped)
  *   out        [T, Hq, Dv] bf16 output;  lse [T, Hq] fp32 output (may be NULL)
@@ -195,6 +212,25 @@ dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, 
  * other bit, DSA_ERR_CUDA if the synchronisation or the copy fails.
  */
 dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* code);
+
+/*
+ * Appends one step's new rows to the paged caches ([A4] 3.3: the indexer's K input is prepared ahead of
+ * the indexer; quantisation per [A1] 1 and [A4] 4): for every query token t (at position p_t, see the
+ * conventions), its indexer key goes to the indexer cache row of p_t and its latent-KV row to the
+ * latent-KV cache row of p_t.  FP8 caches are quantised dynamically per group (the whole indexer key
+ * row; each 128-element latent tile): scale = absmax / 448 (1 for an all-zero group), code =
+ * E4M3(x / scale) rounded to nearest with ties to even and saturated at 448, all in fp32.
+ *   k_new      [T, Di] bf16 new indexer keys, or NULL to leave the indexer cache alone
+ *   kv_new     [T, D] bf16 new latent-KV rows, or NULL to leave the latent-KV cache alone
+ *   k_cache, k_scale   as for dsa_indexer_topk (k_scale: FP8 only, receives the row scales)
+ *   kv_cache   as for dsa_sparse_attn (bf16 rows, or the FP8 row layout)
+ *   workspace  dsa_workspace_size(dims) bytes (only its error word is used)
+ * A token whose page is out of range (DSA_DEVERR_PAGE) or whose position is inconsistent
+ * (DSA_DEVERR_SEQ) writes nothing.  Supported: Di <= 128 and even; D = 576, Dv = 512.
+ */
+dsa_status_t dsa_append_rows(const dsa_dims_t* dims, const void* k_new, const void* kv_new,
+                             const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                             void* k_cache, float* k_scale, void* kv_cache, void* workspace, void* stream);
 
 /* Zeroes the device error word (asynchronously on `stream`). */
 dsa_status_t dsa_clear_device_error(void* workspace, void* stream);

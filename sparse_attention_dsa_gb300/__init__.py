@@ -17,12 +17,14 @@ from ._lib import (  # noqa: F401
     DSA_ERR_TIMEOUT,
     DSA_ERR_UNSUPPORTED,
     DSA_FP8_E4M3,
+    DSA_KV_FP8_ROW_BYTES,
     DSA_OK,
     EXPORTED,
     LIB_PATH,
     DsaDims,
     DsaError,
     abi_version,
+    append_rows,
     clear_device_error,
     fused_decode,
     fused_decode_launches,

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libdsa_gb300.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE, DSA_ERR_TIMEOUT = range(6)
 DSA_BF16, DSA_FP8_E4M3 = 0, 1
+DSA_KV_FP8_ROW_BYTES = 656
 DSA_DEVERR_PAGE, DSA_DEVERR_SEQ, DSA_DEVERR_INDEX, DSA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 EXPORTED = (
@@ -30,6 +31,7 @@ EXPORTED = (
     "dsa_get_device_error",
     "dsa_clear_device_error",
     "dsa_indexer_topk_static",
+    "dsa_append_rows",
 )
 
 
@@ -51,6 +53,7 @@ class DsaDims(ctypes.Structure):
         ("kv_dim", ctypes.c_int32),
         ("v_dim", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
+        ("kv_dtype", ctypes.c_int32),
     ]
 
     def __repr__(self):
@@ -99,6 +102,8 @@ def lib() -> ctypes.CDLL:
             L.dsa_clear_device_error.argtypes = [vp, vp]
             L.dsa_indexer_topk_static.restype = st
             L.dsa_indexer_topk_static.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 11
+            L.dsa_append_rows.restype = st
+            L.dsa_append_rows.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 10
             _lib = L
     return _lib
 
@@ -187,3 +192,11 @@ def get_device_error(workspace, stream=None) -> int:
 
 def clear_device_error(workspace, stream=None):
     _check(lib().dsa_clear_device_error(_ptr(workspace), _stream(stream)))
+
+
+def append_rows(dims, k_new, kv_new, page_table, seq_lens, cu_q_lens, k_cache, k_scale, kv_cache, workspace,
+                stream=None):
+    """dsa_append_rows: write every query token's new indexer key / latent-KV row at its position."""
+    _check(lib().dsa_append_rows(ctypes.byref(dims), _ptr(k_new), _ptr(kv_new), _ptr(page_table), _ptr(seq_lens),
+                                 _ptr(cu_q_lens), _ptr(k_cache), _ptr(k_scale), _ptr(kv_cache), _ptr(workspace),
+                                 _stream(stream)))

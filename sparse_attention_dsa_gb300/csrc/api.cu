@@ -274,6 +274,8 @@ dsa_status_t prepare_sfa(const dsa_dims_t* d, const void* q, const void* kv_cach
         return fail(DSA_ERR_UNSUPPORTED, "sparse attention supports kv_dim 576 / v_dim 512 (got %d / %d)", d->kv_dim,
                     d->v_dim);
     if (d->attn_heads > 128) return fail(DSA_ERR_UNSUPPORTED, "attn_heads must be <= 128 (got %d)", d->attn_heads);
+    if (d->kv_dtype != DSA_BF16 && d->kv_dtype != DSA_FP8_E4M3)
+        return fail(DSA_ERR_INVALID_ARG, "kv_dtype %d is not a dsa_dtype_t", d->kv_dtype);
     if ((int64_t)d->num_pages * 64 > (int64_t)INT32_MAX)
         return fail(DSA_ERR_UNSUPPORTED, "num_pages * 64 must fit in int32 (got %d pages)", d->num_pages);
     if (!(d->softmax_scale > 0.f) || d->softmax_scale > 1e30f)
@@ -309,6 +311,7 @@ dsa_status_t prepare_sfa(const dsa_dims_t* d, const void* q, const void* kv_cach
     p.v_dim = d->v_dim;
     p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
     p.merge = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kErrorWordArea);
+    p.kv_fp8 = d->kv_dtype == DSA_FP8_E4M3 ? 1 : 0;
     L.smem_limit = dev.smem_optin;
     L.num_sms = dev.num_sms;
     {
@@ -391,6 +394,58 @@ dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* 
                              float* lse, void* workspace, void* stream) {
     g_last_error.clear();
     return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream);
+}
+
+dsa_status_t dsa_append_rows(const dsa_dims_t* d, const void* k_new, const void* kv_new, const int32_t* page_table,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, void* k_cache, float* k_scale,
+                             void* kv_cache, void* workspace, void* stream) {
+    g_last_error.clear();
+    dsa_status_t st = check_common(d);
+    if (st) return st;
+    if ((st = check_ptr(k_new, "k_new", false)) || (st = check_ptr(kv_new, "kv_new", false)) ||
+        (st = check_ptr(page_table, "page_table")) || (st = check_ptr(seq_lens, "seq_lens")) ||
+        (st = check_ptr(cu_q_lens, "cu_q_lens")) || (st = check_ptr(workspace, "workspace")))
+        return st;
+    const bool idx_fp8 = d->idx_dtype == DSA_FP8_E4M3, kv_fp8 = d->kv_dtype == DSA_FP8_E4M3;
+    if (k_new) {
+        if (d->idx_dtype != DSA_BF16 && !idx_fp8)
+            return fail(DSA_ERR_INVALID_ARG, "idx_dtype %d is not a dsa_dtype_t", d->idx_dtype);
+        if (d->idx_dim < 2 || d->idx_dim > 128 || (d->idx_dim & 1))
+            return fail(DSA_ERR_UNSUPPORTED, "appending supports an even idx_dim in [2, 128] (got %d)", d->idx_dim);
+        if ((st = check_ptr(k_cache, "k_cache")) || (st = check_ptr(k_scale, "k_scale", idx_fp8))) return st;
+    }
+    if (kv_new) {
+        if (d->kv_dtype != DSA_BF16 && !kv_fp8)
+            return fail(DSA_ERR_INVALID_ARG, "kv_dtype %d is not a dsa_dtype_t", d->kv_dtype);
+        if (d->kv_dim != 576 || d->v_dim != 512)
+            return fail(DSA_ERR_UNSUPPORTED, "appending supports kv_dim 576 / v_dim 512 (got %d / %d)", d->kv_dim,
+                        d->v_dim);
+        if ((st = check_ptr(kv_cache, "kv_cache"))) return st;
+    }
+    if ((int64_t)d->num_pages * 64 > (int64_t)INT32_MAX)
+        return fail(DSA_ERR_UNSUPPORTED, "num_pages * 64 must fit in int32 (got %d pages)", d->num_pages);
+    if (d->total_q == 0 || (!k_new && !kv_new)) return DSA_OK;
+    dsa::AppendParams p;
+    memset(&p, 0, sizeof p);
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.kv_new = static_cast<const uint16_t*>(kv_new);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.cu_q_lens = cu_q_lens;
+    p.k_cache = static_cast<uint8_t*>(k_cache);
+    p.k_scale = k_scale;
+    p.kv_cache = static_cast<uint8_t*>(kv_cache);
+    p.err = static_cast<int32_t*>(workspace);
+    p.batch = d->batch;
+    p.total_q = d->total_q;
+    p.num_pages = d->num_pages;
+    p.max_pages = d->max_pages_per_seq;
+    p.idx_dim = d->idx_dim;
+    p.idx_fp8 = idx_fp8 ? 1 : 0;
+    p.kv_fp8 = kv_fp8 ? 1 : 0;
+    cudaError_t e = dsa::launch_append(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return DSA_OK;
 }
 
 dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,

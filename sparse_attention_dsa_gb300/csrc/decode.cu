@@ -20,7 +20,7 @@
 namespace dsa {
 namespace {
 
-template <int HI, int DI, bool FP8>
+template <int HI, int DI, bool FP8, bool KVFP8>
 __global__ void __launch_bounds__(kThreadsSfa, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap_idx,
                   const IndexerParams ip, const __grid_constant__ CUtensorMap qmap_q, const SfaParams sp) {
@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kThreadsSfa, 1)
     // the cluster's Top-K is written and visible to every CTA of the cluster; nothing of the indexer
     // phase is still in use in shared or tensor memory
     cluster_sync();
-    sfa_cta(qmap_q, sp, smem_raw);
+    sfa_cta<KVFP8>(qmap_q, sp, smem_raw);
 }
 
 struct DecodePlan {
@@ -44,9 +44,9 @@ struct DecodePlan {
 // Chooses the split count P (a cluster of C = 2P CTAs per token) as the attention launcher would, then
 // smaller until the indexer's slice of the scores fits next to at least two pipeline stages and every
 // cluster of the grid can be resident at once.  False when no P works.
-template <int HI, int DI, bool FP8>
+template <int HI, int DI, bool FP8, bool KVFP8>
 bool plan_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, DecodePlan* out) {
-    auto kern = decode_kernel<HI, DI, FP8>;
+    auto kern = decode_kernel<HI, DI, FP8, KVFP8>;
     const int64_t T = SL.params.total_q;
     const int64_t max_ctx = (int64_t)IL.params.max_pages * 64;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
@@ -92,11 +92,11 @@ bool plan_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, DecodePla
     return false;
 }
 
-template <int HI, int DI, bool FP8>
+template <int HI, int DI, bool FP8, bool KVFP8>
 cudaError_t launch_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, cudaStream_t stream) {
     DecodePlan d;
-    if (!plan_decode_variant<HI, DI, FP8>(IL, SL, &d)) return cudaErrorNotSupported;
-    auto kern = decode_kernel<HI, DI, FP8>;
+    if (!plan_decode_variant<HI, DI, FP8, KVFP8>(IL, SL, &d)) return cudaErrorNotSupported;
+    auto kern = decode_kernel<HI, DI, FP8, KVFP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -130,14 +130,21 @@ bool decode_shape_ok(const IndexerLaunch& IL, const SfaLaunch& SL) {
 
 cudaError_t launch_decode(const IndexerLaunch& IL, const SfaLaunch& SL, cudaStream_t stream) {
     if (!decode_shape_ok(IL, SL)) return cudaErrorNotSupported;
-    return IL.fp8 ? launch_decode_variant<64, 128, true>(IL, SL, stream)
-                  : launch_decode_variant<64, 128, false>(IL, SL, stream);
+    const bool kv8 = SL.params.kv_fp8 != 0;
+    if (IL.fp8) return kv8 ? launch_decode_variant<64, 128, true, true>(IL, SL, stream)
+                           : launch_decode_variant<64, 128, true, false>(IL, SL, stream);
+    return kv8 ? launch_decode_variant<64, 128, false, true>(IL, SL, stream)
+               : launch_decode_variant<64, 128, false, false>(IL, SL, stream);
 }
 
 bool decode_single_launch(const IndexerLaunch& IL, const SfaLaunch& SL) {
     if (!decode_shape_ok(IL, SL)) return false;
     DecodePlan d;
-    return IL.fp8 ? plan_decode_variant<64, 128, true>(IL, SL, &d) : plan_decode_variant<64, 128, false>(IL, SL, &d);
+    const bool kv8 = SL.params.kv_fp8 != 0;
+    if (IL.fp8) return kv8 ? plan_decode_variant<64, 128, true, true>(IL, SL, &d)
+                           : plan_decode_variant<64, 128, true, false>(IL, SL, &d);
+    return kv8 ? plan_decode_variant<64, 128, false, true>(IL, SL, &d)
+               : plan_decode_variant<64, 128, false, false>(IL, SL, &d);
 }
 
 }  // namespace dsa

@@ -52,7 +52,7 @@ cudaError_t launch_indexer(const IndexerLaunch& launch, cudaStream_t stream);
 // ---- sparse flash attention --------------------------------------------------------------------------
 struct SfaParams {
     const uint16_t* q;         // [T, Hq, D] bf16 bits
-    const uint16_t* kv_cache;  // [num_pages, 64, D] bf16 bits
+    const uint16_t* kv_cache;  // [num_pages, 64, D] bf16 bits, or FP8 rows of kKvFp8RowBytes (kv_fp8)
     const int32_t* page_table;
     const int32_t* seq_lens;
     const int32_t* cu_q_lens;
@@ -72,6 +72,7 @@ struct SfaParams {
     int32_t splits;    // position splits per query (filled in by the launcher)
     int32_t early_setup;  // launched right behind this library's indexer: only topk comes from it
     float* merge;         // split-merge scratch: sfa_merge_floats_per_cta() floats per CTA of the grid
+    int32_t kv_fp8;       // kv_cache rows are in the FP8 row layout
 };
 
 struct SfaLaunch {
@@ -88,6 +89,31 @@ cudaError_t launch_sfa(const SfaLaunch& launch, cudaStream_t stream);
 // co-residency check), and the most entries one split may hold.
 int sfa_splits(int64_t total_q, int32_t top_k, int num_sms);
 constexpr int kSfaMaxEntries = 2048;
+// FP8 latent-KV row: 512 E4M3 codes (4 tiles of 128), 4 fp32 tile scales, 64 bf16 rotary values
+constexpr int kKvFp8RowBytes = 656;
+constexpr int kKvFp8ScaleOff = 512;
+constexpr int kKvFp8RopeOff = 528;
+
+// ---- appending a step's rows to the paged caches ------------------------------------------------------
+struct AppendParams {
+    const uint16_t* k_new;   // [T, Di] bf16 bits or null
+    const uint16_t* kv_new;  // [T, 576] bf16 bits or null
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const int32_t* cu_q_lens;
+    uint8_t* k_cache;   // bf16 rows of Di, or E4M3 rows of Di bytes (idx_fp8)
+    float* k_scale;     // [num_pages * 64] (idx_fp8)
+    uint8_t* kv_cache;  // bf16 rows of 576, or FP8 rows of kKvFp8RowBytes (kv_fp8)
+    int32_t* err;
+    int32_t batch;
+    int32_t total_q;
+    int32_t num_pages;
+    int32_t max_pages;
+    int32_t idx_dim;
+    int32_t idx_fp8;
+    int32_t kv_fp8;
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
 // Single-launch decode (indexer + Top-K + attention of each token in one cluster, one kernel).  Returns
 // cudaErrorNotSupported, without launching anything, when the sizes do not map one query token to one

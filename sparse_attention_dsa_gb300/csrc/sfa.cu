@@ -10,9 +10,10 @@
 namespace dsa {
 namespace {
 
+template <bool KVFP8>
 __global__ void __launch_bounds__(kThreadsSfa, 1) sfa_kernel(const __grid_constant__ CUtensorMap qmap, const SfaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    sfa_cta(qmap, p, smem_raw);
+    sfa_cta<KVFP8>(qmap, p, smem_raw);
 }
 
 }  // namespace
@@ -37,7 +38,8 @@ size_t sfa_merge_ctas(int64_t total_q, int32_t top_k) {
     return P > 1 ? (size_t)total_q * 2 * P : 0;
 }
 
-// Clusters of `size` CTAs of this kernel that can be resident at once (cached per device and size).
+// Clusters of `size` CTAs of this kernel that can be resident at once (cached per device, variant, size).
+template <bool KVFP8>
 static int max_active_clusters(int size) {
     static int cache[64][2 * kMaxSplits + 1];  // 0 = not queried yet
     int dev = 0;
@@ -56,7 +58,7 @@ static int max_active_clusters(int size) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, sfa_kernel, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, sfa_kernel<KVFP8>, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
@@ -65,21 +67,23 @@ static int max_active_clusters(int size) {
     return c;
 }
 
-cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
+template <bool KVFP8>
+static cudaError_t launch_sfa_variant(const SfaLaunch& L, cudaStream_t stream) {
+    auto kern = sfa_kernel<KVFP8>;
     SfaParams p = L.params;
     static_assert(kQBytes + 2 * kKBufBytes >= kSfaMergeRows * 1024, "split merge rows must fit in the Q and K-part buffers");
     static_assert(kSfaMergeRows >= 128 + kMaxSplits - 1, "P * ceil(128 / P) rows at most");
     if (kSfaSmem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSfaSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSfaSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     // Position splits: grown while the CTAs still fit on the SMs, then shrunk until every cluster of the
     // grid can be resident at once (a second wave of clusters would double the time).
     int P = splits_for(p.total_q, p.top_k, L.num_sms < 256 ? L.num_sms : 256);
     if ((p.top_k + P - 1) / P > kMaxEntries) return cudaErrorInvalidValue;
     const int min_p = splits_for(p.total_q, p.top_k, 0);
-    while (P > min_p && P > 1 && p.total_q > max_active_clusters(2 * P)) --P;
+    while (P > min_p && P > 1 && p.total_q > max_active_clusters<KVFP8>(2 * P)) --P;
     if (P > 1 && (size_t)p.total_q * 2 * P > sfa_merge_ctas(p.total_q, p.top_k)) return cudaErrorInvalidValue;
     p.splits = P;
     p.early_setup = L.after_indexer ? 1 : 0;
@@ -98,7 +102,11 @@ cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = L.after_indexer ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, sfa_kernel, L.qmap, p);
+    return cudaLaunchKernelEx(&cfg, kern, L.qmap, p);
+}
+
+cudaError_t launch_sfa(const SfaLaunch& L, cudaStream_t stream) {
+    return L.params.kv_fp8 ? launch_sfa_variant<true>(L, stream) : launch_sfa_variant<false>(L, stream);
 }
 
 }  // namespace dsa

@@ -124,6 +124,30 @@ __device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* v)
         : "memory");
 }
 
+// Eight E4M3 codes (bytes of c, first code in the lowest byte) times `scale`, rounded to bf16 (eight
+// values, first in the lowest half).  E4M3 -> f16 is exact; the product is taken in fp32.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 c, float scale) {
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t word = (j < 2) ? c.x : c.y;
+        const uint16_t pair = (uint16_t)(word >> (16 * (j & 1)));
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+        float lo, hi;
+        asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(h2));
+        out[j] = f2_to_bf2(lo * scale, hi * scale);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // Atom a (64 dims) of a row belongs to the V part of the CTA that owns value half dvh.
 __device__ __forceinline__ bool is_v_atom(int a, int dvh) { return a >= 4 * dvh && a < 4 * dvh + 4; }
 // Slot of atom a inside its part's buffer.
@@ -133,6 +157,8 @@ __device__ __forceinline__ int part_slot(int a, int dvh) {
 }
 
 // One CTA of the sparse attention (kThreadsSfa threads).  smem_raw: the dynamic shared memory.
+// KVFP8: the latent-KV rows are in the FP8 row layout (dequantised to bf16 by the gather warps).
+template <bool KVFP8>
 __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams& p, uint8_t* smem_raw) {
     // 1024-byte alignment by pointer arithmetic on the shared array (an integer round trip would hide from
     // the compiler that the derived pointers are shared, turning every access into a slower generic one)
@@ -301,6 +327,47 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
             const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
+            if constexpr (KVFP8) {
+                // FP8 rows through registers: every load of the lane's four rows first (the codes of the
+                // part's four latent atoms, their two tile scales, the K part's rotary piece), then the
+                // dequantisation into the same swizzled bf16 layout, then one arrival per lane.
+                static_assert(kRows == 4 * 4 * kKWarps && kKWarps == kVWarps, "four rows per lane");
+                const int a0 = 4 * (v_part ? dvh : 1 - dvh);  // first latent atom of this part
+                const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv_cache);
+                uint2 cd[4][4], sc[4];
+                uint4 rope[4];
+                int32_t rowv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * pw + 16 * k + (lane >> 3);
+                    rowv[k] = rows_s[i * kRows + r];
+                    const uint8_t* src = kvb + (int64_t)(rowv[k] >= 0 ? rowv[k] : 0) * kKvFp8RowBytes;
+                    const bool ok = rowv[k] >= 0;
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2)
+                        cd[k][s2] = ok ? __ldg(reinterpret_cast<const uint2*>(src + (a0 + s2) * 64 + c8 * 8))
+                                       : make_uint2(0, 0);
+                    sc[k] = ok ? __ldg(reinterpret_cast<const uint2*>(src + kKvFp8ScaleOff + 4 * (a0 / 2)))
+                               : make_uint2(0, 0);
+                    rope[k] = (ok && !v_part) ? __ldg(reinterpret_cast<const uint4*>(src + kKvFp8RopeOff + c8 * 16))
+                                              : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * pw + 16 * k + (lane >> 3);
+                    const uint32_t row_base = base + r * 128 + ((c8 ^ (r & 7)) << 4);
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) {
+                        const float scale = __uint_as_float(s2 < 2 ? sc[k].x : sc[k].y);
+                        st_shared_v4(row_base + part_slot(a0 + s2, dvh) * kAtomBytes, e4m3x8_to_bf16x8(cd[k][s2], scale));
+                    }
+                    if (!v_part) st_shared_v4(row_base + part_slot(kAtoms - 1, dvh) * kAtomBytes, rope[k]);
+                }
+                // the MMAs read these bytes through the async proxy
+                fence_proxy_async_smem();
+                mbar_arrive(full);
+                continue;
+            }
 #pragma unroll 1
             for (int r0 = 4 * pw; r0 < kRows; r0 += 4 * nw) {
                 const int r = r0 + (lane >> 3);

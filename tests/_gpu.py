@@ -24,7 +24,8 @@ def dims_for(wl, **override) -> dsa.DsaDims:
                     page_size=wl.page_size, max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads,
                     idx_dim=wl.idx_dim, idx_dtype=dsa.DSA_FP8_E4M3 if wl.idx_fp8 else dsa.DSA_BF16,
                     top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim, v_dim=wl.v_dim,
-                    softmax_scale=wl.softmax_scale)
+                    softmax_scale=wl.softmax_scale,
+                    kv_dtype=dsa.DSA_FP8_E4M3 if getattr(wl, "kv_fp8", False) else dsa.DSA_BF16)
     for k, v in override.items():
         setattr(d, k, v)
     return d

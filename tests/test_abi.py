@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert dsa.abi_version() == 1
+    assert dsa.abi_version() == 2
     for s in range(6):
         assert dsa.status_string(s).startswith("DSA_")
     assert "unknown" in dsa.status_string(99)
@@ -120,6 +120,33 @@ def test_sfa_rejects_bad_arguments(L):
     assert _sfa(_dims(softmax_scale=0.0)) == dsa.DSA_ERR_INVALID_ARG
     assert _sfa(_dims(), out=None) == dsa.DSA_ERR_INVALID_ARG
     assert _sfa(_dims(), lse=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_sfa_rejects_an_unknown_kv_dtype(L):
+    assert _sfa(_dims(kv_dtype=7)) == dsa.DSA_ERR_INVALID_ARG and "kv_dtype" in _msg()
+
+
+def _append(d, **ptrs):
+    p = dict(k_new=FAKE, kv_new=FAKE, page_table=FAKE, seq_lens=FAKE, cu_q_lens=FAKE, k_cache=FAKE, k_scale=None,
+             kv_cache=FAKE, ws=FAKE)
+    p.update(ptrs)
+    return dsa.lib().dsa_append_rows(ctypes.byref(d) if d is not None else None, p["k_new"], p["kv_new"],
+                                     p["page_table"], p["seq_lens"], p["cu_q_lens"], p["k_cache"], p["k_scale"],
+                                     p["kv_cache"], p["ws"], None)
+
+
+def test_append_rejects_bad_arguments(L):
+    assert _append(None) == dsa.DSA_ERR_INVALID_ARG
+    assert _append(_dims(idx_dim=129)) == dsa.DSA_ERR_UNSUPPORTED and "idx_dim" in _msg()
+    assert _append(_dims(idx_dim=63)) == dsa.DSA_ERR_UNSUPPORTED
+    assert _append(_dims(idx_dtype=1)) == dsa.DSA_ERR_INVALID_ARG and "k_scale" in _msg()  # FP8 keys need scales
+    assert _append(_dims(kv_dtype=5)) == dsa.DSA_ERR_INVALID_ARG and "kv_dtype" in _msg()
+    assert _append(_dims(kv_dim=512)) == dsa.DSA_ERR_UNSUPPORTED
+    assert _append(_dims(), kv_cache=None) == dsa.DSA_ERR_INVALID_ARG and "kv_cache" in _msg()
+    assert _append(_dims(), k_new=FAKE + 2) == dsa.DSA_ERR_INVALID_ARG and "aligned" in _msg()
+    # a NULL new-row pointer skips that cache (and its checks); nothing to do returns before any launch
+    assert _append(_dims(), k_new=None, kv_new=None, k_cache=None, kv_cache=None) == dsa.DSA_OK
+    assert _append(_dims(total_q=0)) == dsa.DSA_OK
 
 
 def test_device_error_helpers_validate(L):
