@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0, help="seconds of untimed steps under clock sampling")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="latent-KV cache in the FP8 row layout (one scale per 128 elements of each token)")
     return ap.parse_args(argv)
 
 
@@ -180,7 +182,7 @@ def indexer_bytes(wl) -> int:
 
 def sfa_bytes(wl, topk) -> int:
     sel = int((topk >= 0).sum())
-    gather = sel * wl.kv_dim * 2
+    gather = sel * (wl.kv_cache.shape[-1] if getattr(wl, "kv_fp8", False) else wl.kv_dim * 2)
     qs = wl.total_q * wl.attn_heads * wl.kv_dim * 2
     out = wl.total_q * wl.attn_heads * (wl.v_dim * 2 + 4)
     idx = wl.total_q * wl.top_k * 4
@@ -191,6 +193,12 @@ def sfa_bytes(wl, topk) -> int:
         pages += np.unique(s // 64).shape[0] * 4
     del seq
     return gather + qs + out + idx + pages
+
+
+def workload_name(args) -> str:
+    from gen.workloads import CONFIG_NAMES
+
+    return CONFIG_NAMES[args.config] + ("_kvfp8" if getattr(args, "kv_fp8", False) else "")
 
 
 def measured_peaks():
@@ -271,7 +279,7 @@ def run_reference(args, wl_cfg):
         return 0
     from gen.workloads import CONFIG_NAMES, config
 
-    wl = config(args.config, with_sfa=True)
+    wl = config(args.config, with_sfa=True, kv_fp8=args.kv_fp8)
     cores = oracle_cores()
     n = min(wl.total_q, cores)
     for i in range(args.warmup):
@@ -285,9 +293,9 @@ def run_reference(args, wl_cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": CONFIG_NAMES[args.config], "sample_per_step": f"{n} query tokens"},
+            "config": {"workload": workload_name(args), "sample_per_step": f"{n} query tokens"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{n} query tokens per step of the {CONFIG_NAMES[args.config]} workload"},
+                             "sample": f"{n} query tokens per step of the {workload_name(args)} workload"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -307,7 +315,7 @@ def run_ours(args):
     dist = init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     seed = 1000 + args.config + 7919 * rank
-    wl = config(args.config, seed=seed)
+    wl = config(args.config, seed=seed, kv_fp8=args.kv_fp8)
 
     def up(a):
         if a is None:
@@ -321,7 +329,8 @@ def run_ours(args):
                     page_size=wl.page_size, max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads,
                     idx_dim=wl.idx_dim, idx_dtype=dsa.DSA_FP8_E4M3 if wl.idx_fp8 else dsa.DSA_BF16,
                     top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim, v_dim=wl.v_dim,
-                    softmax_scale=wl.softmax_scale)
+                    softmax_scale=wl.softmax_scale,
+                    kv_dtype=dsa.DSA_FP8_E4M3 if wl.kv_fp8 else dsa.DSA_BF16)
     q_idx, q_scale, w = up(wl.q_idx), up(wl.q_scale), up(wl.w)
     k_cache, k_scale = up(wl.k_cache), up(wl.k_scale)
     q, kv = up(wl.q), up(wl.kv_cache)
@@ -474,7 +483,7 @@ def run_ours(args):
         alg = b_idx if dominant == "indexer" else b_sfa
         dur_ms = idx_ms if dominant == "indexer" else sfa_ms
     achieved = alg / (dur_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(dominant, f"{dominant}_{CONFIG_NAMES[args.config]}.md")
+    traffic = kernel_traffic(dominant, f"{dominant}_{workload_name(args)}.md")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "traffic": traffic, "kernel": dominant, "algorithmic_bytes": alg,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
@@ -483,10 +492,11 @@ def run_ours(args):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8-e4m3 indexer / bf16 attention, fp32 accumulate" if wl.idx_fp8 else
-        "bf16 (fp32 accumulate)",
+        "dtype": ("fp8-e4m3 indexer" if wl.idx_fp8 else "bf16 indexer") +
+        (" / fp8-e4m3 latent-KV cache (128-element tile scales) dequantised to bf16 attention" if wl.kv_fp8 else
+         " / bf16 attention") + ", fp32 accumulate",
         "data": "synthetic (seeded SplitMix64; N(0,1) activations, random page table)",
-        "config": {"workload": CONFIG_NAMES[args.config], "batch_per_gpu": wl.batch, "seq_len": int(wl.seq_lens.max()),
+        "config": {"workload": workload_name(args), "batch_per_gpu": wl.batch, "seq_len": int(wl.seq_lens.max()),
                    "query_tokens_per_gpu": T, "top_k": wl.top_k, "idx_heads": wl.idx_heads, "idx_dim": wl.idx_dim,
                    "attn_heads": wl.attn_heads, "kv_dim": wl.kv_dim, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (indexer K cache and latent-KV cache exceed 129 MB); no flush"},

@@ -321,37 +321,41 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         const int pw = v_part ? gw - kKWarps : gw;  // warp index within its part
         const int nw = v_part ? kVWarps : kKWarps;
         const int c8 = lane & 7;
-        for (int i = 0; i < ntiles; ++i) {
-            const int bsel = i & 1;
-            uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
-            uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
-            const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
-            if constexpr (KVFP8) {
-                // FP8 rows through registers: every load of the lane's four rows first (the codes of the
-                // part's four latent atoms, their two tile scales, the K part's rotary piece), then the
-                // dequantisation into the same swizzled bf16 layout, then one arrival per lane.
-                static_assert(kRows == 4 * 4 * kKWarps && kKWarps == kVWarps, "four rows per lane");
-                const int a0 = 4 * (v_part ? dvh : 1 - dvh);  // first latent atom of this part
-                const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv_cache);
-                uint2 cd[4][4], sc[4];
-                uint4 rope[4];
-                int32_t rowv[4];
+        if constexpr (KVFP8) {
+            // FP8 rows through registers.  The loads of a tile need no buffer, only its stores do: each lane
+            // loads the next tile's data (its four rows: the codes of the part's four latent atoms, their two
+            // tile scales, the K part's rotary piece) right after storing the current one, so the HBM
+            // latency is spent while the buffer is still in use; once it is free, the lane dequantises into
+            // the swizzled bf16 layout, fences for the async proxy and arrives.
+            static_assert(kRows == 4 * 4 * kKWarps && kKWarps == kVWarps, "four rows per lane");
+            const int a0 = 4 * (v_part ? dvh : 1 - dvh);  // first latent atom of this part
+            const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv_cache);
+            uint2 cd[4][4], sc[4];
+            uint4 rope[4];
+            auto load_tile = [&](int i) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int r = 4 * pw + 16 * k + (lane >> 3);
-                    rowv[k] = rows_s[i * kRows + r];
-                    const uint8_t* src = kvb + (int64_t)(rowv[k] >= 0 ? rowv[k] : 0) * kKvFp8RowBytes;
-                    const bool ok = rowv[k] >= 0;
+                    const int32_t row = rows_s[i * kRows + 4 * pw + 16 * k + (lane >> 3)];
+                    const bool ok = row >= 0;
+                    const uint8_t* src = kvb + (int64_t)(ok ? row : 0) * kKvFp8RowBytes;
 #pragma unroll
                     for (int s2 = 0; s2 < 4; ++s2)
                         cd[k][s2] = ok ? __ldg(reinterpret_cast<const uint2*>(src + (a0 + s2) * 64 + c8 * 8))
                                        : make_uint2(0, 0);
                     sc[k] = ok ? __ldg(reinterpret_cast<const uint2*>(src + kKvFp8ScaleOff + 4 * (a0 / 2)))
                                : make_uint2(0, 0);
-                    rope[k] = (ok && !v_part) ? __ldg(reinterpret_cast<const uint4*>(src + kKvFp8RopeOff + c8 * 16))
-                                              : make_uint4(0, 0, 0, 0);
+                    rope[k] = (ok && !v_part)
+                                  ? __ldg(reinterpret_cast<const uint4*>(src + kKvFp8RopeOff + c8 * 16))
+                                  : make_uint4(0, 0, 0, 0);
                 }
+            };
+            if (ntiles > 0) load_tile(0);
+            for (int i = 0; i < ntiles; ++i) {
+                const int bsel = i & 1;
+                uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
+                uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+                const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int r = 4 * pw + 16 * k + (lane >> 3);
@@ -363,31 +367,38 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                     }
                     if (!v_part) st_shared_v4(row_base + part_slot(kAtoms - 1, dvh) * kAtomBytes, rope[k]);
                 }
-                // the MMAs read these bytes through the async proxy
-                fence_proxy_async_smem();
+                fence_proxy_async_smem();  // the MMAs read these bytes through the async proxy
                 mbar_arrive(full);
-                continue;
+                if (i + 1 < ntiles) load_tile(i + 1);
             }
-#pragma unroll 1
-            for (int r0 = 4 * pw; r0 < kRows; r0 += 4 * nw) {
-                const int r = r0 + (lane >> 3);
-                const int32_t row = rows_s[i * kRows + r];
-                const uint16_t* src = p.kv_cache + (int64_t)row * kDim + c8 * 8;
-                const uint32_t row_base = base + r * 128 + ((c8 ^ (r & 7)) << 4);
-#pragma unroll
-                for (int a = 0; a < kAtoms; ++a) {
-                    if (is_v_atom(a, dvh) != v_part) continue;
-                    const uint32_t dst = row_base + part_slot(a, dvh) * kAtomBytes;
-                    if (row >= 0)
-                        cp_async_16(dst, src + a * 64);
-                    else
-                        cp_async_zero16(dst, p.kv_cache);
+        } else {
+            for (int i = 0; i < ntiles; ++i) {
+                const int bsel = i & 1;
+                uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
+                uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+                const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
+    #pragma unroll 1
+                for (int r0 = 4 * pw; r0 < kRows; r0 += 4 * nw) {
+                    const int r = r0 + (lane >> 3);
+                    const int32_t row = rows_s[i * kRows + r];
+                    const uint16_t* src = p.kv_cache + (int64_t)row * kDim + c8 * 8;
+                    const uint32_t row_base = base + r * 128 + ((c8 ^ (r & 7)) << 4);
+    #pragma unroll
+                    for (int a = 0; a < kAtoms; ++a) {
+                        if (is_v_atom(a, dvh) != v_part) continue;
+                        const uint32_t dst = row_base + part_slot(a, dvh) * kAtomBytes;
+                        if (row >= 0)
+                            cp_async_16(dst, src + a * 64);
+                        else
+                            cp_async_zero16(dst, p.kv_cache);
+                    }
                 }
+                // every lane signals once its own copies have landed; the warp moves on to the next tile at once
+                cp_async_mbar_arrive(full);
             }
-            // every lane signals once its own copies have landed; the warp moves on to the next tile at once
-            cp_async_mbar_arrive(full);
+            cp_async_wait_all();
         }
-        cp_async_wait_all();
     }
     else if (warp == 1) {
         // ---------------- MMA issuer: S(i) = Q K(i)^T, then O += P(i-1) V(i-1) ----------------
