@@ -110,8 +110,10 @@ const char* dsa_last_error_message(void);
 /*
  * Bytes of device workspace the compute calls need for `dims`: 256 bytes whose first int32 is the
  * device error word, then (when the attention kernel may split one query's positions across several
- * CTAs: few query tokens) scratch for merging those splits, 129 KiB per CTA of the largest grid it may
- * use (at most about 33 MiB).  The caller allocates it once (16-byte aligned, as from cudaMalloc),
+ * CTAs: few query tokens) scratch for merging those splits, 137 KiB per CTA of the largest grid it may
+ * use (at most about 33 MiB), then (when max_q_len == 1) T x K int32 through which the single-launch
+ * dsa_fused_decode hands the physical cache rows of the Top-K from its indexer phase to its attention
+ * phase.  The caller allocates it once (16-byte aligned, as from cudaMalloc),
  * zero-fills at least the first 256 bytes before first use, and passes the same buffer to later calls;
  * the error word latches until dsa_clear_device_error().  Returns 0 when dims is NULL.  Calls that may
  * overlap on the GPU need separate workspaces.

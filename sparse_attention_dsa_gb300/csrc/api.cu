@@ -83,6 +83,15 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Workspace layout: the error word area, the attention kernel's split-merge scratch for the largest grid
+// it may use, then (decode shapes: one query token per sequence) the physical rows of the Top-K that the
+// single-launch decode kernel hands from its indexer phase to its attention phase.
+size_t merge_bytes(int64_t T, int32_t K) { return dsa::sfa_merge_ctas(T, K) * dsa::kSfaMergeFloatsPerCta * sizeof(float); }
+size_t decode_rows_bytes(const dsa_dims_t* d) {
+    if (d->max_q_len != 1 || d->total_q <= 0 || d->top_k <= 0) return 0;
+    return ((size_t)d->total_q * (size_t)d->top_k * sizeof(int32_t) + 15) / 16 * 16;
+}
+
 dsa_status_t check_ptr(const void* p, const char* name, bool required = true) {
     if (!p) return required ? fail(DSA_ERR_INVALID_ARG, "%s is NULL", name) : DSA_OK;
     if (!aligned16(p)) return fail(DSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
@@ -374,10 +383,9 @@ const char* dsa_last_error_message(void) { return g_last_error.c_str(); }
 
 size_t dsa_workspace_size(const dsa_dims_t* dims) {
     if (!dims) return 0;
-    // the error word area, then the attention kernel's split-merge scratch for the largest grid it may use
     const int64_t T = dims->total_q > 0 ? dims->total_q : 0;
     const int32_t K = dims->top_k > 0 ? dims->top_k : 0;
-    return dsa::kErrorWordArea + dsa::sfa_merge_ctas(T, K) * dsa::kSfaMergeFloatsPerCta * sizeof(float);
+    return dsa::kErrorWordArea + merge_bytes(T, K) + decode_rows_bytes(dims);
 }
 
 dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
@@ -462,11 +470,20 @@ dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const f
     st = prepare_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, &SL, &ls);
     if (st) return st;
     if (!li || !ls) return DSA_OK;  // no query token
-    // one launch when every query token can have a cluster of its own for both phases
+    // one launch when every query token can have a cluster of its own for both phases; its indexer phase
+    // hands the Top-K's physical rows to its attention phase through the workspace
+    if (decode_rows_bytes(dims) > 0) {
+        int32_t* rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + dsa::kErrorWordArea +
+                                                   merge_bytes(dims->total_q, dims->top_k));
+        IL.params.rows_out = rows;
+        SL.params.rows_in = rows;
+    }
     cudaError_t e = dsa::launch_decode(IL, SL, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) return DSA_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode launch");
     // otherwise the indexer, then the attention kernel as its programmatic dependent
+    IL.params.rows_out = nullptr;
+    SL.params.rows_in = nullptr;
     if ((st = launch_indexer_checked(IL, stream))) return st;
     return launch_sfa_checked(SL, stream, true);
 }

@@ -214,12 +214,27 @@ __device__ void exchange_pass(const uint32_t* keys, int n, uint32_t prefix, int 
 template <int NT>
 __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, uint32_t* sbuf, int n,
                                int K, int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
-                               SelectSmem& S) {
+                               SelectSmem& S, const int32_t* pages, int32_t* rows_row) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (visible <= K) {  // every visible position is kept: 0..p in order, then -1
-        const int per = (K + (int)C - 1) / (int)C;
-        const int lo = (int)rank * per, hi = min(K, lo + per);
-        for (int s = lo + tid; s < hi; s += NT) out_row[s] = (int64_t)s < visible ? s : -1;
+    // physical cache row of local key i (its page from this CTA's page list), -1 for a missing page
+    auto row_of = [&](int i) -> int32_t {
+        const int32_t pg = pages[i >> 6];
+        return pg >= 0 ? pg * kPage + (i & (kPage - 1)) : -1;
+    };
+    if (visible <= K) {
+        // every visible position is kept: 0..p in order (each CTA writes those of its own range), then -1
+        const int64_t own_hi = min((int64_t)range_start + n, visible);
+        for (int64_t s = (int64_t)range_start + tid; s < own_hi; s += NT) {
+            out_row[s] = (int32_t)s;
+            if (rows_row) rows_row[s] = row_of((int)(s - range_start));
+        }
+        const int pad = K - (int)visible;
+        const int per = (pad + (int)C - 1) / (int)C;
+        const int lo = (int)visible + (int)rank * per, hi = min(K, lo + per);
+        for (int s = lo + tid; s < hi; s += NT) {
+            out_row[s] = -1;
+            if (rows_row) rows_row[s] = -1;
+        }
         return;
     }
     uint32_t remaining = (uint32_t)K, prefix = 0, bstar = 0;
@@ -539,7 +554,10 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             if ((sm >> e) & 1u) {
-                if (pos < (uint32_t)K) out_row[pos] = range_start + i + e;
+                if (pos < (uint32_t)K) {
+                    out_row[pos] = range_start + i + e;
+                    if (rows_row) rows_row[pos] = row_of(i + e);
+                }
                 ++pos;
             }
         }
@@ -839,7 +857,8 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         // the smem stage ring is idle once every CTA has scored: it holds the select's fallback exchange space
         cluster_select<NT>(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, reinterpret_cast<uint32_t*>(a_tiles),
                        n_keys, p.top_k, visible,
-                       p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel);
+                       p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel, pages_s,
+                       p.rows_out ? p.rows_out + (int64_t)(t0 + q) * p.top_k : nullptr);
     }
     // No cluster barrier here: every remote access is a histogram push, and the pushes of a pass complete
     // before that pass's barrier, so after the last pass no CTA touches another's shared memory.

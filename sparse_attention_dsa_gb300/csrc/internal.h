@@ -28,6 +28,7 @@ struct IndexerParams {
     int32_t blocks_per_seq;  // ceil(max_q_len / qb)
     int32_t chunk;           // positions per CTA (multiple of 128)
     int32_t stages;          // filled in by the launcher
+    int32_t* rows_out;       // [T, K] physical cache row of every selected position (-1 for padding), or null
 };
 
 struct IndexerLaunch {
@@ -73,6 +74,7 @@ struct SfaParams {
     int32_t early_setup;  // launched right behind this library's indexer: only topk comes from it
     float* merge;         // split-merge scratch: sfa_merge_floats_per_cta() floats per CTA of the grid
     int32_t kv_fp8;       // kv_cache rows are in the FP8 row layout
+    const int32_t* rows_in;  // [T, K] physical rows of topk written by the indexer phase in the same launch, or null
 };
 
 struct SfaLaunch {

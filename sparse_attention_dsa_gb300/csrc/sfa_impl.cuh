@@ -186,8 +186,9 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
     if (tid == 0) prefetch_tensormap(&qmap);
     if (!p.early_setup) grid_dependency_wait();
     int32_t ent[kEntPerThread];
+    // the split's Top-K entries, or (rows_in: written by the indexer phase of this launch) their physical rows
     auto load_entries = [&]() {
-        const int32_t* sel = p.topk + (int64_t)t * p.top_k + e0;
+        const int32_t* sel = (p.rows_in ? p.rows_in : p.topk) + (int64_t)t * p.top_k + e0;
 #pragma unroll
         for (int k = 0; k < kEntPerThread; ++k) {
             const int e = tid + k * kThreadsSfa;
@@ -287,6 +288,20 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         grid_dependency_wait();
         load_entries();
     }
+    if (p.rows_in) {
+        // physical rows already: only a bounds check (a row that no valid selection can produce is an error)
+#pragma unroll
+        for (int k = 0; k < kEntPerThread; ++k) {
+            const int e = tid + k * kThreadsSfa;
+            if (e >= ntiles * kRows) continue;
+            int32_t row = ent[k];
+            if (row < -1 || (int64_t)row >= (int64_t)p.num_pages * 64) {
+                if (dvh == 0) raise_error(p.err, DSA_DEVERR_PAGE);
+                row = -1;
+            }
+            rows_s[e] = row;
+        }
+    } else {
     int32_t pg[kEntPerThread];
     {
         const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
@@ -310,6 +325,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             }
         }
         rows_s[e] = row;
+    }
     }
     __syncthreads();
 

@@ -51,11 +51,15 @@ def test_workspace_size(L):
     assert L.dsa_workspace_size(None) == 0
     # few query tokens and K = 2048: the attention may split positions and needs merge scratch
     # (137 KiB per CTA of the largest grid it may use)
+    # (decode shapes, one query token per sequence: plus T x K int32 for the single-launch kernel's rows)
+    rows = lambda T, K: (T * K * 4 + 15) // 16 * 16
     ws = dsa.workspace_size(_dims(top_k=2048))
-    assert ws > 256 and (ws - 256) % (136 * 256 * 4 + 256 * 4) == 0
-    # one 64-row tile per query (K = 16), or many query tokens: no splits, just the error word area
-    assert dsa.workspace_size(_dims(top_k=16)) == 256
-    assert dsa.workspace_size(_dims(batch=4096, total_q=4096, top_k=2048)) == 256
+    assert ws - 256 - rows(2, 2048) > 0 and (ws - 256 - rows(2, 2048)) % (136 * 256 * 4 + 256 * 4) == 0
+    # one 64-row tile per query (K = 16), or many query tokens: no splits
+    assert dsa.workspace_size(_dims(top_k=16)) == 256 + rows(2, 16)
+    assert dsa.workspace_size(_dims(batch=4096, total_q=4096, top_k=2048)) == 256 + rows(4096, 2048)
+    # several query tokens per sequence: no single-launch kernel, so no rows area
+    assert dsa.workspace_size(_dims(max_q_len=2, total_q=4, top_k=16)) == 256
 
 
 def test_fused_decode_launches_host_cases(L):
