@@ -133,6 +133,25 @@ def quantize_e4m3_rows(x_bf16: np.ndarray):
     return codes, scales
 
 
+def quantize_mx_rows(x_bf16: np.ndarray, group: int = 32):
+    """MX (OCP microscaling) E4M3 quantisation of a bf16-bits array [..., cols] with one E8M0 scale per
+    `group` consecutive elements: shared exponent floor(log2(absmax)) - 8 (the largest E4M3 exponent),
+    clamped to the E8M0 range; codes = E4M3(x / 2^shared) with saturation; an all-zero group gets
+    exponent 0 (byte 127).  Returns (codes uint8 [..., cols], scale bytes uint8 [..., cols / group])."""
+    x = bf16_to_f32(np.ascontiguousarray(x_bf16, dtype=np.uint16))
+    cols = x.shape[-1]
+    assert cols % group == 0
+    g = x.reshape(-1, cols // group, group)
+    amax = np.max(np.abs(g), axis=-1)
+    _, e = np.frexp(amax)  # amax = f * 2^e, f in [0.5, 1): floor(log2(amax)) = e - 1
+    shared = np.where(amax > 0, e.astype(np.int64) - 1 - 8, 0)
+    shared = np.clip(shared, -127, 127)
+    y = (g / np.ldexp(np.float32(1.0), shared)[..., None].astype(np.float32)).astype(np.float32)
+    codes = e4m3_encode_array(y).reshape(x.shape)
+    scales = (shared + 127).astype(np.uint8).reshape(*x.shape[:-1], cols // group)
+    return codes, scales
+
+
 def bf16_to_f32(x: np.ndarray) -> np.ndarray:
     """Bit-exact widening of bf16 bits to float32 (a shift; used for inspection and fixtures)."""
     return (np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)

@@ -25,6 +25,8 @@ Recipe (identical for every config and for the small test cases):
   have their indexer key multiplied by 4 (exact in bf16).
 * FP8 inputs: bf16 values quantised per row (one row = one token's 128-d key, or one (token, head)
   query row) with scale = absmax/448.
+* MXFP8 indexer inputs (idx_mx): the same bf16 rows quantised with one E8M0 scale per 32 elements
+  (shared exponent floor(log2(absmax)) - 8); scales are bytes [..., Di / 32].
 * FP8 latent-KV cache (kv_fp8): the same bf16 rows, each 128-dim tile of the leading Dv dims quantised
   with its own absmax/448 scale; row layout 656 bytes = Dv codes, Dv/128 fp32 scales, the remaining
   (rotary) dims as bf16.
@@ -44,6 +46,7 @@ from . import (
     paged_normal_bf16,
     permutation,
     quantize_e4m3_rows,
+    quantize_mx_rows,
     sample_without_replacement,
     stream_key,
     uniform_f32,
@@ -81,6 +84,7 @@ class Workload:
     kv_cache: Optional[np.ndarray] = None  # bf16 bits uint16 [P, 64, kv_dim], or uint8 [P, 64, 656] (kv_fp8)
     notes: dict = field(default_factory=dict)
     kv_fp8: bool = False
+    idx_mx: bool = False  # with idx_fp8: q/k scales are E8M0 bytes per 32 elements (MXFP8)
 
     @property
     def batch(self) -> int:
@@ -140,7 +144,7 @@ def make_workload(name: str, seed: int, seq_lens: Sequence[int], q_lens: Sequenc
                   idx_dim: int, idx_fp8: bool, top_k: int, attn_heads: int, kv_dim: int = 576, v_dim: int = 512,
                   w_hi: float = 1.0, salient_frac: float = 0.0, salient_mult: float = 4.0,
                   page_size: int = PAGE_SIZE, softmax_scale: Optional[float] = None, with_sfa: bool = True,
-                  page_seed: Optional[int] = None, kv_fp8: bool = False) -> Workload:
+                  page_seed: Optional[int] = None, kv_fp8: bool = False, idx_mx: bool = False) -> Workload:
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     q_lens = np.asarray(q_lens, dtype=np.int32)
     assert seq_lens.shape == q_lens.shape
@@ -170,7 +174,10 @@ def make_workload(name: str, seed: int, seq_lens: Sequence[int], q_lens: Sequenc
             n_sal += m
         notes["salient_rows"] = n_sal
     q_scale = k_scale = None
-    if idx_fp8:
+    if idx_fp8 and idx_mx:
+        q_idx, q_scale = quantize_mx_rows(q_idx)
+        k_cache, k_scale = quantize_mx_rows(k_cache)
+    elif idx_fp8:
         q_idx, q_scale = quantize_e4m3_rows(q_idx)
         k_cache, k_scale = quantize_e4m3_rows(k_cache)
     q = kv = None
@@ -185,7 +192,7 @@ def make_workload(name: str, seed: int, seq_lens: Sequence[int], q_lens: Sequenc
                     num_pages=num_pages, idx_heads=idx_heads, idx_dim=idx_dim, idx_fp8=idx_fp8, q_idx=q_idx,
                     q_scale=q_scale, w=w, k_cache=k_cache, k_scale=k_scale, top_k=top_k, attn_heads=attn_heads,
                     kv_dim=kv_dim, v_dim=v_dim, softmax_scale=float(softmax_scale), q=q, kv_cache=kv, notes=notes,
-                    kv_fp8=bool(kv_fp8 and with_sfa))
+                    kv_fp8=bool(kv_fp8 and with_sfa), idx_mx=bool(idx_fp8 and idx_mx))
 
 
 def kv_fp8_row_bytes(kv_dim: int = 576, v_dim: int = 512) -> int:

@@ -81,6 +81,8 @@ def lib():
             L.oracle_index_scores_batch.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 9 + [i32, ctypes.c_int64, vp]
             L.oracle_sparse_attn.restype = ctypes.c_int
             L.oracle_sparse_attn.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 7 + [i32, vp, vp, vp]
+            L.oracle_e8m0_value.restype = ctypes.c_double
+            L.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
             L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
             L.oracle_quantize_group.restype = None
@@ -101,7 +103,7 @@ def _p(a):
 def _dims(wl) -> _Dims:
     return _Dims(batch=wl.batch, total_q=wl.total_q, num_pages=wl.num_pages, page_size=wl.page_size,
                  max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads, idx_dim=wl.idx_dim,
-                 idx_fp8=1 if wl.idx_fp8 else 0, top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim,
+                 idx_fp8=(2 if getattr(wl, "idx_mx", False) else 1) if wl.idx_fp8 else 0, top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim,
                  v_dim=wl.v_dim, kv_fp8=1 if getattr(wl, "kv_fp8", False) else 0, softmax_scale=wl.softmax_scale)
 
 
@@ -206,3 +208,8 @@ def append(wl, k_new=None, kv_new=None):
                                   _p(wl.cu_q_lens), _p(k_cache), _p(k_scale), _p(kv_cache))
     _check(rc)
     return k_cache, k_scale, kv_cache
+
+
+def e8m0_value(e: int) -> float:
+    """OCP MX E8M0 scale byte: 2^(e - 127); 0xFF is NaN."""
+    return float(lib().oracle_e8m0_value(e))

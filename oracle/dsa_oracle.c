@@ -24,6 +24,9 @@
  * The articles describe the steps in prose and print no formula.  Readings used here:
  *  - index score  I[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d])   (no softmax, no bias);
  *  - FP8 inputs are E4M3 codes (OCP OFP8 definition) times one fp32 scale per row, applied literally;
+ *  - MXFP8 inputs ([A1] section 1 and [A4] section 4.1: microscaled FP8, one scale per group of 32
+ *    elements): E4M3 codes times one E8M0 scale per 32 consecutive elements of a row (OCP MX
+ *    definition: the byte e means 2^(e - 127), 0xFF is NaN), applied literally;
  *  - query t of sequence b (n_b new tokens, L_b cached tokens including them) sits at position
  *    p = L_b - n_b + j and sees positions 0..p (causal, itself included);
  *  - Top-K orders by score descending, then position ascending; with fewer than K visible positions
@@ -57,7 +60,8 @@ typedef struct {
     int32_t max_pages_per_seq;
     int32_t idx_heads;
     int32_t idx_dim;
-    int32_t idx_fp8; /* 0: q_idx/k_idx are bf16 bits; 1: E4M3 codes with fp32 row scales */
+    int32_t idx_fp8; /* 0: q_idx/k_idx are bf16 bits; 1: E4M3 codes with fp32 row scales;
+                        2: E4M3 codes with one E8M0 scale byte per 32 elements (MXFP8) */
     int32_t top_k;
     int32_t attn_heads;
     int32_t kv_dim;
@@ -147,6 +151,12 @@ static double kv_elem(const oracle_dims* d, const void* kv_cache, int64_t row, i
     return oracle_bf16_value(bits);
 }
 
+/* OCP MX E8M0 scale: 2^(e - 127); 0xFF is NaN. */
+double oracle_e8m0_value(uint8_t e) {
+    if (e == 0xFF) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
 /* Sequence of query token t and its causal position. */
 static int query_locate(const oracle_dims* d, const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t t,
                         int32_t* b_out, int64_t* p_out) {
@@ -175,6 +185,11 @@ static int page_row(const oracle_dims* d, const int32_t* page_table, int32_t b, 
 }
 
 static double idx_elem(const oracle_dims* d, const void* base, const float* scales, int64_t row, int32_t col) {
+    if (d->idx_fp8 == 2) {  /* scales: E8M0 bytes [rows][idx_dim / 32] */
+        const uint8_t* p = (const uint8_t*)base;
+        const uint8_t* e = (const uint8_t*)scales;
+        return oracle_e4m3_value(p[row * d->idx_dim + col]) * oracle_e8m0_value(e[row * (d->idx_dim / 32) + col / 32]);
+    }
     if (d->idx_fp8) {
         const uint8_t* p = (const uint8_t*)base;
         return oracle_e4m3_value(p[row * d->idx_dim + col]) * (double)scales[row];
@@ -436,6 +451,7 @@ int oracle_append_rows(const oracle_dims* d, const uint16_t* k_new, const uint16
                        const int32_t* seq_lens, const int32_t* cu_q_lens, void* k_cache, float* k_scale,
                        void* kv_cache) {
     int err = 0;
+    if (k_new && d->idx_fp8 == 2) return ORC_BAD_ARG; /* appending MXFP8 keys is not defined here */
     float* x = (float*)malloc(sizeof(float) * (size_t)(d->idx_dim > d->kv_dim ? d->idx_dim : d->kv_dim));
     if (!x) return ORC_NOMEM;
     for (int32_t t = 0; t < d->total_q; ++t) {

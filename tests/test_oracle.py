@@ -408,3 +408,59 @@ def test_append_writes_each_token_row_at_its_position(fp8):
                 continue
             assert np.array_equal(k_cache[page, slot], wl.k_cache[page, slot])
             assert np.array_equal(kv_cache[page, slot], wl.kv_cache[page, slot])
+
+
+# ---------------------------------------------------------------------------------------------------
+# MXFP8 indexer inputs (E4M3 codes, one E8M0 scale per 32 elements)
+# ---------------------------------------------------------------------------------------------------
+
+
+def test_e8m0_decoder_matches_torch_for_every_byte():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).double().numpy()
+    ours = np.array([oracle.e8m0_value(int(c)) for c in codes])
+    assert np.isnan(ours[255]) and np.isnan(ref[255])
+    assert np.array_equal(ours[:255], ref[:255])
+    assert ours[127] == 1.0 and ours[0] == 2.0 ** -127 and ours[254] == 2.0 ** 127
+
+
+def test_generator_mx_quantiser_follows_the_definition():
+    from gen import quantize_mx_rows
+
+    rng = np.random.default_rng(12)
+    x = (rng.normal(0, 1, (40, 128)) * 2.0 ** rng.integers(-20, 20, (40, 1))).astype(np.float32)
+    x[3, 32:64] = 0.0  # an all-zero group
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    codes, scales = quantize_mx_rows(bits)
+    xf = bf16_to_f32(bits).reshape(40, 4, 32)
+    amax = np.abs(xf).max(axis=-1)
+    shared = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1))) - 8, 0).astype(np.int64)
+    assert np.array_equal(scales.astype(np.int64) - 127, shared)
+    # x / 2^shared can reach 512: the MX conversion saturates at the largest E4M3 value (torch gives NaN)
+    y = (xf / np.float32(2.0) ** shared[..., None]).reshape(40, 128)
+    ref = _torch_e4m3(np.clip(y, -448.0, 448.0))
+    assert np.any(np.abs(y) > 448)
+    assert np.array_equal(codes, ref)
+    assert np.all(codes[3, 32:64] == 0) and scales[3, 1] == 127
+
+
+def test_mx_scores_equal_bf16_scores_on_the_same_values():
+    wl = _small(idx_fp8=True, idx_mx=True, idx_heads=3, idx_dim=64, top_k=16)
+    assert wl.q_scale.shape == (wl.total_q, 3, 2) and wl.k_scale.shape[-1] == 2
+    # the same values decoded by torch (codes as float8_e4m3fn, scales as float8_e8m0fnu), exact in bf16
+    def decode(codes, scales):
+        v = _torch_e4m3_value(codes.reshape(-1, codes.shape[-1]))
+        s = torch.from_numpy(np.ascontiguousarray(scales.reshape(-1, scales.shape[-1]))).view(
+            torch.float8_e8m0fnu).double().numpy()
+        v = v * np.repeat(s, 32, axis=1)
+        b = (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        assert np.array_equal(bf16_to_f32(b).astype(np.float64), v)
+        return b.reshape(codes.shape)
+    scores_mx = [oracle.index_scores(wl, t) for t in range(wl.total_q)]
+    top_mx = oracle.indexer_topk(wl)[0]
+    wl.q_idx, wl.k_cache = decode(wl.q_idx, wl.q_scale), decode(wl.k_cache, wl.k_scale)
+    wl.q_scale = wl.k_scale = None
+    wl.idx_fp8, wl.idx_mx = False, False
+    for t in range(wl.total_q):
+        assert np.array_equal(oracle.index_scores(wl, t), scores_mx[t])
+    assert np.array_equal(oracle.indexer_topk(wl)[0], top_mx)
