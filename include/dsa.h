@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 typedef enum {
     DSA_OK = 0,
@@ -58,9 +58,12 @@ typedef enum {
 } dsa_status_t;
 
 typedef enum {
-    DSA_BF16 = 0,     /* bfloat16 */
-    DSA_FP8_E4M3 = 1  /* OCP OFP8 E4M3 codes times fp32 scales: indexer rows with one scale per row
-                         ([A3] 3.1); latent-KV rows in the FP8 row layout below */
+    DSA_BF16 = 0,       /* bfloat16 */
+    DSA_FP8_E4M3 = 1,   /* OCP OFP8 E4M3 codes times fp32 scales: indexer rows with one scale per row
+                           ([A3] 3.1); latent-KV rows in the FP8 row layout below */
+    DSA_MXFP8_E4M3 = 2  /* indexer only: E4M3 codes with one E8M0 scale byte per 32 consecutive elements
+                           of a row (OCP MX: the byte e means 2^(e - 127); [A1] 1, [A4] 4.1 "MXFP8,
+                           per-group 32") */
 } dsa_dtype_t;
 
 /*
@@ -126,21 +129,23 @@ size_t dsa_workspace_size(const dsa_dims_t* dims);
  * and keep the K positions with the largest I (ties: the lower position wins).  The scores stay on
  * chip; only the selected positions are written.  With FP8 inputs, q_idx[t,h,:] and k[s,:] are the
  * codes times their row scales.
- *   q_idx        [T, Hi, Di]  bf16, or E4M3 codes (uint8) when dims->idx_dtype == DSA_FP8_E4M3
- *   q_scale      [T, Hi]      fp32 row scales of q_idx (FP8 only; NULL for bf16)
+ *   q_idx        [T, Hi, Di]  bf16, or E4M3 codes (uint8) when dims->idx_dtype is DSA_FP8_E4M3 or
+ *                DSA_MXFP8_E4M3
+ *   q_scale      [T, Hi] fp32 row scales of q_idx (DSA_FP8_E4M3), [T, Hi, Di/32] E8M0 bytes
+ *                (DSA_MXFP8_E4M3), NULL for bf16
  *   w            [T, Hi]      fp32 head weights
  *   k_cache      [num_pages, 64, Di]  paged indexer keys, same dtype as q_idx
- *   k_scale      [num_pages, 64]      fp32 row scales of k_cache (FP8 only; NULL for bf16)
+ *   k_scale      [num_pages, 64] fp32 row scales of k_cache (DSA_FP8_E4M3), [num_pages, 64, Di/32] E8M0
+ *                bytes (DSA_MXFP8_E4M3), NULL for bf16
  *   page_table   [B, max_pages_per_seq] int32;  seq_lens [B] int32;  cu_q_lens [B+1] int32
  *   topk_idx     [T, K] int32 output: the selected positions of each query in ascending order; when
  *                fewer than K positions are visible all of them are kept and the rest is -1.
  *   workspace    dsa_workspace_size(dims) bytes (see above)
- * Supported: (Hi, Di) = (4, 64) or (64, 128) in bf16, (64, 128) in FP8; K <= 4096; per sequence at
- * most 2 query tokens when max_pages_per_seq * 64 > 65536, else at most 4 (DSA_ERR_UNSUPPORTED
- * otherwise).
+ * Supported: (Hi, Di) = (4, 64) or (64, 128) in bf16, (64, 128) in FP8 and MXFP8; K <= 4096 (MXFP8 runs
+ * one query token per thread-block cluster, any number per sequence).
  */
-dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
-                              const void* k_cache, const float* k_scale, const int32_t* page_table,
+dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
+                              const void* k_cache, const void* k_scale, const int32_t* page_table,
                               const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx,
                               void* workspace, void* stream);
 
@@ -173,8 +178,8 @@ dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* 
  * attention launched as a programmatic dependent of the indexer.  dsa_fused_decode_launches() tells
  * which.
  */
-dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
-                              const void* k_cache, const float* k_scale, const void* q, const void* kv_cache,
+dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
+                              const void* k_cache, const void* k_scale, const void* q, const void* kv_cache,
                               const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
                               int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream);
 
@@ -203,8 +208,8 @@ int32_t dsa_fused_decode_launches(const dsa_dims_t* dims);
  * GPU (different streams, or different host threads) race on it.  Nothing is allocated: no cudaMalloc,
  * cudaFree or allocating library routine is called.
  */
-dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, const float* q_scale,
-                                     const float* w, const void* k_cache, const float* k_scale,
+dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, const void* q_scale,
+                                     const float* w, const void* k_cache, const void* k_scale,
                                      const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
                                      int32_t* topk_idx, int32_t* device_error, void* stream);
 
@@ -224,7 +229,8 @@ dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* 
  * E4M3(x / scale) rounded to nearest with ties to even and saturated at 448, all in fp32.
  *   k_new      [T, Di] bf16 new indexer keys, or NULL to leave the indexer cache alone
  *   kv_new     [T, D] bf16 new latent-KV rows, or NULL to leave the latent-KV cache alone
- *   k_cache, k_scale   as for dsa_indexer_topk (k_scale: FP8 only, receives the row scales)
+ *   k_cache, k_scale   as for dsa_indexer_topk (k_scale: FP8 only, receives the fp32 row scales;
+ *                      MXFP8 keys are not appended: DSA_ERR_UNSUPPORTED)
  *   kv_cache   as for dsa_sparse_attn (bf16 rows, or the FP8 row layout)
  *   workspace  dsa_workspace_size(dims) bytes (only its error word is used)
  * A token whose page is out of range (DSA_DEVERR_PAGE) or whose position is inconsistent
@@ -232,7 +238,7 @@ dsa_status_t dsa_get_device_error(const void* workspace, void* stream, int32_t* 
  */
 dsa_status_t dsa_append_rows(const dsa_dims_t* dims, const void* k_new, const void* kv_new,
                              const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
-                             void* k_cache, float* k_scale, void* kv_cache, void* workspace, void* stream);
+                             void* k_cache, void* k_scale, void* kv_cache, void* workspace, void* stream);
 
 /* Zeroes the device error word (asynchronously on `stream`). */
 dsa_status_t dsa_clear_device_error(void* workspace, void* stream);

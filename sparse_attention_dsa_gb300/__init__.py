@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     DSA_ERR_UNSUPPORTED,
     DSA_FP8_E4M3,
     DSA_KV_FP8_ROW_BYTES,
+    DSA_MXFP8_E4M3,
     DSA_OK,
     EXPORTED,
     LIB_PATH,

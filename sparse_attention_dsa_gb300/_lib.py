@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa_gb300.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE, DSA_ERR_TIMEOUT = range(6)
-DSA_BF16, DSA_FP8_E4M3 = 0, 1
+DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
 DSA_KV_FP8_ROW_BYTES = 656
 DSA_DEVERR_PAGE, DSA_DEVERR_SEQ, DSA_DEVERR_INDEX, DSA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 

@@ -120,12 +120,19 @@ constexpr int kMaxClusterSize = 16;
 dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::IndexerLaunch* L) {
     if (d->idx_heads < 1 || d->idx_dim < 1)
         return fail(DSA_ERR_INVALID_ARG, "idx_heads and idx_dim must be >= 1 (got %d, %d)", d->idx_heads, d->idx_dim);
-    if (d->idx_dtype != DSA_BF16 && d->idx_dtype != DSA_FP8_E4M3)
+    if (d->idx_dtype != DSA_BF16 && d->idx_dtype != DSA_FP8_E4M3 && d->idx_dtype != DSA_MXFP8_E4M3)
         return fail(DSA_ERR_INVALID_ARG, "idx_dtype %d is not a dsa_dtype_t", d->idx_dtype);
-    const bool fp8 = d->idx_dtype == DSA_FP8_E4M3;
+    const bool mx = d->idx_dtype == DSA_MXFP8_E4M3;
+    const bool fp8 = d->idx_dtype == DSA_FP8_E4M3 || mx;  // one-byte codes
+    const int quant = mx ? 2 : fp8 ? 1 : 0;
     const int64_t max_ctx = (int64_t)d->max_pages_per_seq * 64;
     int qb_max;
-    if (!fp8 && d->idx_heads == 4 && d->idx_dim == 64)
+    if (mx) {
+        if (d->idx_heads != 64 || d->idx_dim != 128)
+            return fail(DSA_ERR_UNSUPPORTED, "MXFP8 indexer supports 64 heads of 128 dims (got %d, %d)", d->idx_heads,
+                        d->idx_dim);
+        qb_max = 1;
+    } else if (!fp8 && d->idx_heads == 4 && d->idx_dim == 64)
         qb_max = 4;
     else if (d->idx_heads == 64 && d->idx_dim == 128)
         qb_max = (!fp8 && max_ctx <= 65536) ? 4 : 2;
@@ -143,10 +150,10 @@ dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::Index
     int qb = 0, c_min = 0;
     for (int min_stages = 3; min_stages >= 2 && c_min == 0; --min_stages)
         for (int q = qb_want; q >= 1 && c_min == 0; q /= 2) {
-            if (dsa::indexer_variant_n(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, q) == 0) continue;
+            if (dsa::indexer_variant_n(d->idx_heads, d->idx_dim, quant, q) == 0) continue;
             for (int C = 1; C <= kMaxClusterSize; C *= 2)
                 if (chunk_for(C) <= INT32_MAX &&
-                    dsa::indexer_smem_estimate(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, q, min_stages, (int)chunk_for(C),
+                    dsa::indexer_smem_estimate(d->idx_heads, d->idx_dim, quant, q, min_stages, (int)chunk_for(C),
                                                C) <= (size_t)dev.smem_optin) {
                     qb = q;
                     c_min = C;
@@ -168,6 +175,7 @@ dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::Index
     L->idx_heads = d->idx_heads;
     L->idx_dim = d->idx_dim;
     L->fp8 = fp8;
+    L->mx = mx;
     L->smem_limit = dev.smem_optin;
     L->check_occupancy = true;
     dsa::IndexerParams& p = L->params;
@@ -222,20 +230,26 @@ dsa_status_t prepare_indexer(const dsa_dims_t* d, const void* q_idx, const float
     *launch = false;
     dsa_status_t st = check_common(d);
     if (st) return st;
-    const bool fp8 = d->idx_dtype == DSA_FP8_E4M3;
+    const bool fp8 = d->idx_dtype == DSA_FP8_E4M3 || d->idx_dtype == DSA_MXFP8_E4M3;
     if ((st = check_ptr(q_idx, "q_idx")) || (st = check_ptr(w, "w")) || (st = check_ptr(k_cache, "k_cache")) ||
         (st = check_ptr(page_table, "page_table")) || (st = check_ptr(seq_lens, "seq_lens")) ||
         (st = check_ptr(cu_q_lens, "cu_q_lens")) || (st = check_ptr(topk_idx, "topk_idx")) ||
         (st = check_ptr(workspace, "workspace")))
         return st;
     if (fp8 && ((st = check_ptr(q_scale, "q_scale")) || (st = check_ptr(k_scale, "k_scale")))) return st;
+    // argument checks that need no device come before the device query
+    if (d->idx_dtype != DSA_BF16 && d->idx_dtype != DSA_FP8_E4M3 && d->idx_dtype != DSA_MXFP8_E4M3)
+        return fail(DSA_ERR_INVALID_ARG, "idx_dtype %d is not a dsa_dtype_t", d->idx_dtype);
+    if (d->idx_dtype == DSA_MXFP8_E4M3 && (d->idx_heads != 64 || d->idx_dim != 128))
+        return fail(DSA_ERR_UNSUPPORTED, "MXFP8 indexer supports 64 heads of 128 dims (got %d, %d)", d->idx_heads,
+                    d->idx_dim);
     DeviceInfo dev;
     if ((st = device_info(&dev))) return st;
     dsa::IndexerLaunch& L = *Lout;
     memset(&L, 0, sizeof L);
     if ((st = plan_indexer(d, dev, &L))) return st;
     if (d->total_q == 0) return DSA_OK;
-    const int n_cols = dsa::indexer_variant_n(d->idx_heads, d->idx_dim, fp8 ? 1 : 0, L.params.qb);
+    const int n_cols = dsa::indexer_variant_n(d->idx_heads, d->idx_dim, L.mx ? 2 : fp8 ? 1 : 0, L.params.qb);
     if ((st = encode_indexer_maps(d, q_idx, k_cache, n_cols, &L))) return st;
     dsa::IndexerParams& p = L.params;
     p.q_scale = fp8 ? q_scale : nullptr;
@@ -388,13 +402,14 @@ size_t dsa_workspace_size(const dsa_dims_t* dims) {
     return dsa::kErrorWordArea + merge_bytes(T, K) + decode_rows_bytes(dims);
 }
 
-dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
-                              const void* k_cache, const float* k_scale, const int32_t* page_table,
+dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
+                              const void* k_cache, const void* k_scale, const int32_t* page_table,
                               const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace,
                               void* stream) {
     g_last_error.clear();
-    return run_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx, workspace,
-                       stream);
+    // the scale arrays are fp32 (DSA_FP8_E4M3) or E8M0 bytes (DSA_MXFP8_E4M3); the kernels read them by type
+    return run_indexer(dims, q_idx, static_cast<const float*>(q_scale), w, k_cache, static_cast<const float*>(k_scale),
+                       page_table, seq_lens, cu_q_lens, topk_idx, workspace, stream);
 }
 
 dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* kv_cache, const int32_t* page_table,
@@ -405,7 +420,7 @@ dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* 
 }
 
 dsa_status_t dsa_append_rows(const dsa_dims_t* d, const void* k_new, const void* kv_new, const int32_t* page_table,
-                             const int32_t* seq_lens, const int32_t* cu_q_lens, void* k_cache, float* k_scale,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, void* k_cache, void* k_scale,
                              void* kv_cache, void* workspace, void* stream) {
     g_last_error.clear();
     dsa_status_t st = check_common(d);
@@ -416,6 +431,8 @@ dsa_status_t dsa_append_rows(const dsa_dims_t* d, const void* k_new, const void*
         return st;
     const bool idx_fp8 = d->idx_dtype == DSA_FP8_E4M3, kv_fp8 = d->kv_dtype == DSA_FP8_E4M3;
     if (k_new) {
+        if (d->idx_dtype == DSA_MXFP8_E4M3)
+            return fail(DSA_ERR_UNSUPPORTED, "appending MXFP8 indexer keys is not supported");
         if (d->idx_dtype != DSA_BF16 && !idx_fp8)
             return fail(DSA_ERR_INVALID_ARG, "idx_dtype %d is not a dsa_dtype_t", d->idx_dtype);
         if (d->idx_dim < 2 || d->idx_dim > 128 || (d->idx_dim & 1))
@@ -441,7 +458,7 @@ dsa_status_t dsa_append_rows(const dsa_dims_t* d, const void* k_new, const void*
     p.seq_lens = seq_lens;
     p.cu_q_lens = cu_q_lens;
     p.k_cache = static_cast<uint8_t*>(k_cache);
-    p.k_scale = k_scale;
+    p.k_scale = static_cast<float*>(k_scale);
     p.kv_cache = static_cast<uint8_t*>(kv_cache);
     p.err = static_cast<int32_t*>(workspace);
     p.batch = d->batch;
@@ -456,11 +473,13 @@ dsa_status_t dsa_append_rows(const dsa_dims_t* d, const void* k_new, const void*
     return DSA_OK;
 }
 
-dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const float* q_scale, const float* w,
-                              const void* k_cache, const float* k_scale, const void* q, const void* kv_cache,
+dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const void* q_scale_v, const float* w,
+                              const void* k_cache, const void* k_scale_v, const void* q, const void* kv_cache,
                               const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
                               int32_t* topk_idx, void* out, float* lse, void* workspace, void* stream) {
     g_last_error.clear();
+    const float* q_scale = static_cast<const float*>(q_scale_v);  // fp32, or E8M0 bytes (MXFP8)
+    const float* k_scale = static_cast<const float*>(k_scale_v);
     dsa::IndexerLaunch IL;
     dsa::SfaLaunch SL;
     bool li = false, ls = false;

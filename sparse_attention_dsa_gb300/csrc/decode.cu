@@ -20,13 +20,13 @@
 namespace dsa {
 namespace {
 
-template <int HI, int DI, bool FP8, bool KVFP8>
+template <int HI, int DI, bool FP8, bool MX, bool KVFP8>
 __global__ void __launch_bounds__(kThreadsSfa, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap_idx,
                   const IndexerParams ip, const __grid_constant__ CUtensorMap qmap_q, const SfaParams sp) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // (the attention phase allocates tensor memory again, so the indexer phase keeps the allocation permit)
-    indexer_cta<HI, DI, 1, FP8, kThreadsSfa, false>(kmap, qmap_idx, ip, smem_raw);
+    indexer_cta<HI, DI, 1, FP8, kThreadsSfa, false, MX>(kmap, qmap_idx, ip, smem_raw);
     // shared memory this thread wrote is next written by the attention phase's copies (async proxy)
     fence_proxy_async_smem();
     // the cluster's Top-K is written and visible to every CTA of the cluster; nothing of the indexer
@@ -44,9 +44,9 @@ struct DecodePlan {
 // Chooses the split count P (a cluster of C = 2P CTAs per token) as the attention launcher would, then
 // smaller until the indexer's slice of the scores fits next to at least two pipeline stages and every
 // cluster of the grid can be resident at once.  False when no P works.
-template <int HI, int DI, bool FP8, bool KVFP8>
+template <int HI, int DI, bool FP8, bool MX, bool KVFP8>
 bool plan_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, DecodePlan* out) {
-    auto kern = decode_kernel<HI, DI, FP8, KVFP8>;
+    auto kern = decode_kernel<HI, DI, FP8, MX, KVFP8>;
     const int64_t T = SL.params.total_q;
     const int64_t max_ctx = (int64_t)IL.params.max_pages * 64;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
@@ -60,8 +60,8 @@ bool plan_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, DecodePla
         const int64_t chunk = (per + 127) / 128 * 128;
         if (chunk > INT32_MAX) continue;
         int stages = kMaxStages;
-        while (stages > 2 && indexer_smem_bytes<HI, DI, 1, FP8>(stages, (int)chunk, C) > (size_t)SL.smem_limit) --stages;
-        const size_t idx_smem = indexer_smem_bytes<HI, DI, 1, FP8>(stages, (int)chunk, C);
+        while (stages > 2 && indexer_smem_bytes<HI, DI, 1, FP8, MX>(stages, (int)chunk, C) > (size_t)SL.smem_limit) --stages;
+        const size_t idx_smem = indexer_smem_bytes<HI, DI, 1, FP8, MX>(stages, (int)chunk, C);
         const size_t smem = idx_smem > kSfaSmem ? idx_smem : kSfaSmem;
         if (smem > (size_t)SL.smem_limit) continue;
         if (P > 1 && (size_t)T * 2 * P > sfa_merge_ctas(T, SL.params.top_k)) continue;
@@ -92,11 +92,11 @@ bool plan_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, DecodePla
     return false;
 }
 
-template <int HI, int DI, bool FP8, bool KVFP8>
+template <int HI, int DI, bool FP8, bool MX, bool KVFP8>
 cudaError_t launch_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, cudaStream_t stream) {
     DecodePlan d;
-    if (!plan_decode_variant<HI, DI, FP8, KVFP8>(IL, SL, &d)) return cudaErrorNotSupported;
-    auto kern = decode_kernel<HI, DI, FP8, KVFP8>;
+    if (!plan_decode_variant<HI, DI, FP8, MX, KVFP8>(IL, SL, &d)) return cudaErrorNotSupported;
+    auto kern = decode_kernel<HI, DI, FP8, MX, KVFP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -131,20 +131,24 @@ bool decode_shape_ok(const IndexerLaunch& IL, const SfaLaunch& SL) {
 cudaError_t launch_decode(const IndexerLaunch& IL, const SfaLaunch& SL, cudaStream_t stream) {
     if (!decode_shape_ok(IL, SL)) return cudaErrorNotSupported;
     const bool kv8 = SL.params.kv_fp8 != 0;
-    if (IL.fp8) return kv8 ? launch_decode_variant<64, 128, true, true>(IL, SL, stream)
-                           : launch_decode_variant<64, 128, true, false>(IL, SL, stream);
-    return kv8 ? launch_decode_variant<64, 128, false, true>(IL, SL, stream)
-               : launch_decode_variant<64, 128, false, false>(IL, SL, stream);
+    if (IL.mx) return kv8 ? launch_decode_variant<64, 128, true, true, true>(IL, SL, stream)
+                          : launch_decode_variant<64, 128, true, true, false>(IL, SL, stream);
+    if (IL.fp8) return kv8 ? launch_decode_variant<64, 128, true, false, true>(IL, SL, stream)
+                           : launch_decode_variant<64, 128, true, false, false>(IL, SL, stream);
+    return kv8 ? launch_decode_variant<64, 128, false, false, true>(IL, SL, stream)
+               : launch_decode_variant<64, 128, false, false, false>(IL, SL, stream);
 }
 
 bool decode_single_launch(const IndexerLaunch& IL, const SfaLaunch& SL) {
     if (!decode_shape_ok(IL, SL)) return false;
     DecodePlan d;
     const bool kv8 = SL.params.kv_fp8 != 0;
-    if (IL.fp8) return kv8 ? plan_decode_variant<64, 128, true, true>(IL, SL, &d)
-                           : plan_decode_variant<64, 128, true, false>(IL, SL, &d);
-    return kv8 ? plan_decode_variant<64, 128, false, true>(IL, SL, &d)
-               : plan_decode_variant<64, 128, false, false>(IL, SL, &d);
+    if (IL.mx) return kv8 ? plan_decode_variant<64, 128, true, true, true>(IL, SL, &d)
+                          : plan_decode_variant<64, 128, true, true, false>(IL, SL, &d);
+    if (IL.fp8) return kv8 ? plan_decode_variant<64, 128, true, false, true>(IL, SL, &d)
+                           : plan_decode_variant<64, 128, true, false, false>(IL, SL, &d);
+    return kv8 ? plan_decode_variant<64, 128, false, false, true>(IL, SL, &d)
+               : plan_decode_variant<64, 128, false, false, false>(IL, SL, &d);
 }
 
 }  // namespace dsa

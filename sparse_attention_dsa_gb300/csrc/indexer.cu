@@ -11,23 +11,22 @@
 namespace dsa {
 namespace {
 
-template <int HI, int DI, int QB, bool FP8>
+template <int HI, int DI, int QB, bool FP8, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                         const IndexerParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    indexer_cta<HI, DI, QB, FP8, kThreads, true>(kmap, qmap, p, smem_raw);
+    indexer_cta<HI, DI, QB, FP8, kThreads, true, MX>(kmap, qmap, p, smem_raw);
 }
 
-template <int HI, int DI, int QB, bool FP8>
+template <int HI, int DI, int QB, bool FP8, bool MX = false>
 cudaError_t launch_variant(const IndexerLaunch& L, cudaStream_t stream) {
-    using Cfg = IdxCfg<HI, DI, QB, FP8>;
-    auto kern = indexer_topk_kernel<HI, DI, QB, FP8>;
+    auto kern = indexer_topk_kernel<HI, DI, QB, FP8, MX>;
     const int chunk = L.params.chunk;
     // choose the number of pipeline stages from the shared-memory budget
     int stages = kMaxStages;
-    while (stages > 2 && indexer_smem_bytes<HI, DI, QB, FP8>(stages, chunk, L.cluster) > (size_t)L.smem_limit) --stages;
-    const size_t smem = indexer_smem_bytes<HI, DI, QB, FP8>(stages, chunk, L.cluster);
+    while (stages > 2 && indexer_smem_bytes<HI, DI, QB, FP8, MX>(stages, chunk, L.cluster) > (size_t)L.smem_limit) --stages;
+    const size_t smem = indexer_smem_bytes<HI, DI, QB, FP8, MX>(stages, chunk, L.cluster);
     if (smem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
     IndexerParams prm = L.params;
     prm.stages = stages;
@@ -60,12 +59,16 @@ cudaError_t launch_variant(const IndexerLaunch& L, cudaStream_t stream) {
 
 int indexer_variant_n(int idx_heads, int idx_dim, int fp8, int qb) {
     // UMMA N of the variant that serves these shapes (0 = unsupported)
+    if (fp8 == 2) return (idx_heads == 64 && idx_dim == 128 && qb == 1) ? 64 : 0;
     if (!fp8 && idx_heads == 4 && idx_dim == 64 && qb >= 1 && qb <= 4) return 16;
     if (idx_heads == 64 && idx_dim == 128 && (qb == 1 || qb == 2 || (qb == 4 && !fp8))) return 64 * qb;
     return 0;
 }
 
 size_t indexer_smem_estimate(int idx_heads, int idx_dim, int fp8, int qb, int stages, int chunk, int cluster) {
+    if (fp8 == 2)
+        return (idx_heads == 64 && idx_dim == 128 && qb == 1) ? indexer_smem_bytes<64, 128, 1, true, true>(stages, chunk, cluster)
+                                                               : ~size_t(0);
     if (!fp8 && idx_heads == 4 && idx_dim == 64) return indexer_smem_bytes<4, 64, 4, false>(stages, chunk, cluster);
     if (idx_heads == 64 && idx_dim == 128) {
         if (fp8) {
@@ -82,6 +85,10 @@ size_t indexer_smem_estimate(int idx_heads, int idx_dim, int fp8, int qb, int st
 
 cudaError_t launch_indexer(const IndexerLaunch& L, cudaStream_t stream) {
     const int qb = L.params.qb;
+    if (L.mx) {
+        if (L.idx_heads == 64 && L.idx_dim == 128 && qb == 1) return launch_variant<64, 128, 1, true, true>(L, stream);
+        return cudaErrorInvalidValue;
+    }
     if (!L.fp8 && L.idx_heads == 4 && L.idx_dim == 64) return launch_variant<4, 64, 4, false>(L, stream);
     if (L.idx_heads == 64 && L.idx_dim == 128) {
         if (L.fp8) {

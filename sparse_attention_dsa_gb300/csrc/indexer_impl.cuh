@@ -42,10 +42,15 @@ constexpr int kTileM = 128;  // positions per tile (two pages)
 constexpr int kPage = 64;
 constexpr int kMaxCluster = 16;
 
-template <int HI, int DI, int QB, bool FP8>
+// MX: FP8 with one E8M0 scale per 32 elements of a row (MXFP8): every 32-element K step gets its own
+// accumulator, and the epilogue applies the two groups' scales before the ReLU.
+template <int HI, int DI, int QB, bool FP8, bool MX = false>
 struct IdxCfg {
+    static_assert(!MX || (FP8 && QB == 1 && DI % 32 == 0), "MXFP8: FP8 codes, one query per work item");
     static constexpr int kNReal = HI * QB;
     static constexpr int kN = kNReal < 16 ? 16 : ((kNReal + 15) / 16) * 16;  // UMMA N for M = 128
+    static constexpr int kGroups = MX ? DI / 32 : 1;     // accumulators per tile (scale groups along K)
+    static constexpr int kAccCols = kN * kGroups;        // TMEM columns of one tile's accumulators
     static constexpr int kElem = FP8 ? 1 : 2;
     static constexpr int kRowBytes = DI * kElem;
     static constexpr int kAtoms = kRowBytes / 128;  // 128-byte swizzle atoms along K
@@ -54,9 +59,10 @@ struct IdxCfg {
     static constexpr int kMmaK = FP8 ? 32 : 16;  // elements per UMMA
     static constexpr int kKSteps = DI / kMmaK;
     // accumulator buffers in TMEM: enough that the MMA issuer rarely waits for the epilogue
-    static constexpr int kAccBufs = (4 * kN) <= 512 ? 4 : 2;
-    static constexpr int kTmemCols = (kAccBufs * kN) <= 32 ? 32 : (kAccBufs * kN) <= 64 ? 64
-                                     : (kAccBufs * kN) <= 128 ? 128 : (kAccBufs * kN) <= 256 ? 256 : 512;
+    static constexpr int kAccBufs = (4 * kAccCols) <= 512 ? 4 : 2;
+    static constexpr int kTmemCols = (kAccBufs * kAccCols) <= 32 ? 32 : (kAccBufs * kAccCols) <= 64 ? 64
+                                     : (kAccBufs * kAccCols) <= 128 ? 128 : (kAccBufs * kAccCols) <= 256 ? 256 : 512;
+    static_assert(kAccBufs * kAccCols <= 512, "TMEM columns");
     static constexpr uint32_t kIdesc = make_idesc(128, kN, FP8 ? 0u : 1u, FP8 ? 0u : 1u, 0u, 0u);
     static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
     // the select's fallback exchange space (2 x C x 256 words) lives in the stage ring (at least 2 stages)
@@ -99,6 +105,13 @@ struct CtrlSmem {
     int32_t issued;    // tiles issued by the producer
     int32_t qwaited;
 };
+
+// E8M0 scale byte e as the float 2^(e - 127) (e = 0: 2^-127, a subnormal; e = 255: NaN).
+__device__ __forceinline__ float e8m0_factor(uint32_t e) {
+    if (e == 0u) return __uint_as_float(0x00400000u);
+    if (e == 255u) return __uint_as_float(0x7FC00000u);
+    return __uint_as_float(e << 23);
+}
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -573,10 +586,10 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
 // roles use warps 0-5; all NT threads take part in the select).  smem_raw: the dynamic shared memory.
 // LAST_TMEM: no later phase of the kernel allocates tensor memory, so the allocation permit is given up
 // after this CTA's allocation.
-template <int HI, int DI, int QB, bool FP8, int NT, bool LAST_TMEM>
+template <int HI, int DI, int QB, bool FP8, int NT, bool LAST_TMEM, bool MX = false>
 __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p,
                                             uint8_t* smem_raw) {
-    using Cfg = IdxCfg<HI, DI, QB, FP8>;
+    using Cfg = IdxCfg<HI, DI, QB, FP8, MX>;
     static_assert(NT % 32 == 0 && NT >= 256 && NT / 32 <= kMaxWarps, "thread count of the indexer body");
     // 1024-byte alignment for the swizzled operand tiles, by pointer arithmetic on the shared array (an
     // integer round trip would hide from the compiler that the derived pointers are shared, turning every
@@ -587,7 +600,8 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     uint8_t* q_tile = a_tiles + (size_t)S * Cfg::kStageBytes;  // kQBytes
     uint32_t* keys = reinterpret_cast<uint32_t*>(q_tile + Cfg::kQBytes);  // QB * chunk
     float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
-    int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64, padded to 16 bytes
+    float* qf_s = w_s + Cfg::kN;  // MX: 2^(e - 127) of every (head, group) query scale, [kN][kGroups]
+    int32_t* pages_s = reinterpret_cast<int32_t*>(qf_s + (MX ? Cfg::kN * Cfg::kGroups : 0));  // chunk / 64, padded
     // everything after the page list is read with 16-byte vector loads: keep it 16-byte aligned
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + page_words(p.chunk));  // QB x 256
     uint32_t* allh = hist0 + QB * 256;                                      // C x 768 (select exchange)
@@ -648,9 +662,17 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         if (c < nq * HI) {
             const int64_t idx = (int64_t)(t0 + c / HI) * HI + (c % HI);
             wv = p.w[idx];
-            if (FP8) wv *= p.q_scale[idx];
+            if (FP8 && !MX) wv *= p.q_scale[idx];
         }
         w_s[c] = wv;
+    }
+    if constexpr (MX) {
+        // the query's scale bytes [T, Hi, kGroups] as factors 2^(e - 127)
+        const uint8_t* qe = reinterpret_cast<const uint8_t*>(p.q_scale);
+        for (int i = tid; i < Cfg::kN * Cfg::kGroups; i += NT) {
+            const int c = i / Cfg::kGroups, g = i % Cfg::kGroups;
+            qf_s[i] = c < nq * HI ? e8m0_factor(qe[((int64_t)t0 * HI + c) * Cfg::kGroups + g]) : 0.f;
+        }
     }
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -742,7 +764,9 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                         const int atom = kb / 128, off = kb % 128;
                         const uint64_t ad = smem_desc(a_base + atom * (kTileM * 128) + off, 16, 1024, kSwizzle128B);
                         const uint64_t bd = smem_desc(q_base + atom * (Cfg::kN * 128) + off, 16, 1024, kSwizzle128B);
-                        if (FP8)
+                        if (MX)  // one 32-element scale group per K step: its own accumulator
+                            umma_f8_ss(tmem + ab * Cfg::kAccCols + k * Cfg::kN, ad, bd, Cfg::kIdesc, 0u);
+                        else if (FP8)
                             umma_f8_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
                         else
                             umma_f16_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
@@ -767,13 +791,42 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 const int pos = range_start + local;
                 const int32_t pg = pages_s[2 * i + (row >> 6)];
                 float ksc = 1.f;
-                if (FP8 && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
+                uint32_t kexp = 0;  // MX: the key row's scale bytes (group g in byte g)
+                if (MX && pg >= 0) kexp = __ldg(reinterpret_cast<const uint32_t*>(p.k_scale) + (int64_t)pg * kPage + (row & 63));
+                else if (FP8 && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err))) break;
                 tc_fence_after();
                 float acc[QB];
 #pragma unroll
                 for (int q = 0; q < QB; ++q) acc[q] = 0.f;
-                if constexpr (HI % 32 == 0) {
+                if constexpr (MX) {
+                    // every head's dot product is the sum over its scale groups of 2^(eq + ek) times the
+                    // group's accumulator; the ReLU and the head weight come after that sum
+                    static_assert(Cfg::kGroups == 4, "four 32-element groups per 128-dim key");
+                    float f[4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) f[g] = e8m0_factor((kexp >> (8 * g)) & 255u);
+                    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int c0 = 0; c0 < HI; c0 += 16) {
+                        float v[4][16];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + ab * Cfg::kAccCols + g * Cfg::kN + c0, v[g]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) tmem_regs_ready(v[g]);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float4 qf = reinterpret_cast<const float4*>(qf_s)[c0 + j];
+                            float x = v[0][j] * (qf.x * f[0]);
+                            x = fmaf(v[1][j], qf.y * f[1], x);
+                            x = fmaf(v[2][j], qf.z * f[2], x);
+                            x = fmaf(v[3][j], qf.w * f[3], x);
+                            part[j & 7] = fmaf(w_s[c0 + j], fmaxf(x, 0.f), part[j & 7]);
+                        }
+                    }
+                    acc[0] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                } else if constexpr (HI % 32 == 0) {
                     // One query's heads, 32 columns per TMEM wait, in a rolled loop: the code stays small
                     // (it shares the instruction cache with the MMA warp), eight independent partial sums
                     // keep the FMA chains short, and the weights come four at a time.
@@ -829,7 +882,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
 #pragma unroll
                 for (int q = 0; q < QB; ++q) {
                     uint32_t key = 0;
-                    if (q < nq && pg >= 0 && (int64_t)pos <= pq[q]) key = score_key(FP8 ? acc[q] * ksc : acc[q]);
+                    if (q < nq && pg >= 0 && (int64_t)pos <= pq[q]) key = score_key((FP8 && !MX) ? acc[q] * ksc : acc[q]);
                     keys[q * p.chunk + local] = key;
                     // top-byte histogram for the first radix pass (warp-aggregated)
                     const uint32_t bin = key >> 24;
@@ -876,10 +929,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     }
 }
 
-template <int HI, int DI, int QB, bool FP8>
+template <int HI, int DI, int QB, bool FP8, bool MX = false>
 size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
-    using Cfg = IdxCfg<HI, DI, QB, FP8>;
+    using Cfg = IdxCfg<HI, DI, QB, FP8, MX>;
     return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
+           (MX ? (size_t)Cfg::kN * Cfg::kGroups * 4 : 0) +
            (size_t)page_words(chunk) * 4 + (size_t)(QB + 3 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
            64;
 }

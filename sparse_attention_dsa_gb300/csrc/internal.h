@@ -40,14 +40,15 @@ struct IndexerLaunch {
     int idx_heads;
     int idx_dim;
     bool fp8;
+    bool mx;         // FP8 with one E8M0 scale per 32 elements (q_scale / k_scale hold scale bytes)
     int smem_limit;  // opt-in dynamic shared memory per block
     bool check_occupancy;
 };
 
 // UMMA N of the kernel variant serving (Hi, Di, dtype, qb), 0 when no variant exists.
-int indexer_variant_n(int idx_heads, int idx_dim, int fp8, int qb);
+int indexer_variant_n(int idx_heads, int idx_dim, int fp8, int qb);  // fp8: 0 bf16, 1 row scales, 2 MXFP8
 // Dynamic shared memory of that variant for the given pipeline depth, positions per CTA and cluster size.
-size_t indexer_smem_estimate(int idx_heads, int idx_dim, int fp8, int qb, int stages, int chunk, int cluster);
+size_t indexer_smem_estimate(int idx_heads, int idx_dim, int fp8, int qb, int stages, int chunk, int cluster);  // fp8 as above
 cudaError_t launch_indexer(const IndexerLaunch& launch, cudaStream_t stream);
 
 // ---- sparse flash attention --------------------------------------------------------------------------

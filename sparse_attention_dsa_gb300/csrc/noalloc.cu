@@ -56,8 +56,8 @@ dsa_status_t scratch_address(void** out) {
 
 }  // namespace
 
-extern "C" dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, const float* q_scale,
-                                                const float* w, const void* k_cache, const float* k_scale,
+extern "C" dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, const void* q_scale,
+                                                const float* w, const void* k_cache, const void* k_scale,
                                                 const int32_t* page_table, const int32_t* seq_lens,
                                                 const int32_t* cu_q_lens, int32_t* topk_idx, int32_t* device_error,
                                                 void* stream) {

@@ -22,7 +22,9 @@ def ensure_built():
 def dims_for(wl, **override) -> dsa.DsaDims:
     d = dsa.DsaDims(batch=wl.batch, total_q=wl.total_q, max_q_len=wl.max_q_len, num_pages=wl.num_pages,
                     page_size=wl.page_size, max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads,
-                    idx_dim=wl.idx_dim, idx_dtype=dsa.DSA_FP8_E4M3 if wl.idx_fp8 else dsa.DSA_BF16,
+                    idx_dim=wl.idx_dim,
+                    idx_dtype=(dsa.DSA_MXFP8_E4M3 if getattr(wl, "idx_mx", False) else dsa.DSA_FP8_E4M3)
+                    if wl.idx_fp8 else dsa.DSA_BF16,
                     top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim, v_dim=wl.v_dim,
                     softmax_scale=wl.softmax_scale,
                     kv_dtype=dsa.DSA_FP8_E4M3 if getattr(wl, "kv_fp8", False) else dsa.DSA_BF16)

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert dsa.abi_version() == 2
+    assert dsa.abi_version() == 3
     for s in range(6):
         assert dsa.status_string(s).startswith("DSA_")
     assert "unknown" in dsa.status_string(99)
@@ -124,6 +124,15 @@ def test_sfa_rejects_bad_arguments(L):
     assert _sfa(_dims(softmax_scale=0.0)) == dsa.DSA_ERR_INVALID_ARG
     assert _sfa(_dims(), out=None) == dsa.DSA_ERR_INVALID_ARG
     assert _sfa(_dims(), lse=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_mxfp8_indexer_shape_limits(L):
+    # MXFP8 needs both scale arrays, and serves 64 heads of 128 dims only
+    assert _indexer(_dims(idx_dtype=2)) == dsa.DSA_ERR_INVALID_ARG and "scale" in _msg()
+    assert _indexer(_dims(idx_dtype=2, idx_heads=4, idx_dim=64), q_scale=FAKE, k_scale=FAKE) == dsa.DSA_ERR_UNSUPPORTED
+    assert "MXFP8" in _msg()
+    assert _indexer(_dims(idx_dtype=3), q_scale=FAKE, k_scale=FAKE) == dsa.DSA_ERR_INVALID_ARG
+    assert _append(_dims(idx_dtype=2), k_scale=FAKE) == dsa.DSA_ERR_UNSUPPORTED and "MXFP8" in _msg()
 
 
 def test_sfa_rejects_an_unknown_kv_dtype(L):
