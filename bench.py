@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0, help="seconds of untimed steps under clock sampling")
+    ap.add_argument("--idx-mx", action="store_true",
+                    help="MXFP8 indexer inputs (E4M3 codes, one E8M0 scale per 32 elements)")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="latent-KV cache in the FP8 row layout (one scale per 128 elements of each token)")
     return ap.parse_args(argv)
@@ -198,7 +200,8 @@ def sfa_bytes(wl, topk) -> int:
 def workload_name(args) -> str:
     from gen.workloads import CONFIG_NAMES
 
-    return CONFIG_NAMES[args.config] + ("_kvfp8" if getattr(args, "kv_fp8", False) else "")
+    return (CONFIG_NAMES[args.config] + ("_mxfp8" if getattr(args, "idx_mx", False) else "") +
+            ("_kvfp8" if getattr(args, "kv_fp8", False) else ""))
 
 
 def measured_peaks():
@@ -279,7 +282,7 @@ def run_reference(args, wl_cfg):
         return 0
     from gen.workloads import CONFIG_NAMES, config
 
-    wl = config(args.config, with_sfa=True, kv_fp8=args.kv_fp8)
+    wl = config(args.config, with_sfa=True, kv_fp8=args.kv_fp8, idx_mx=args.idx_mx)
     cores = oracle_cores()
     n = min(wl.total_q, cores)
     for i in range(args.warmup):
@@ -315,7 +318,7 @@ def run_ours(args):
     dist = init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     seed = 1000 + args.config + 7919 * rank
-    wl = config(args.config, seed=seed, kv_fp8=args.kv_fp8)
+    wl = config(args.config, seed=seed, kv_fp8=args.kv_fp8, idx_mx=args.idx_mx)
 
     def up(a):
         if a is None:
@@ -327,7 +330,8 @@ def run_ours(args):
 
     d = dsa.DsaDims(batch=wl.batch, total_q=wl.total_q, max_q_len=wl.max_q_len, num_pages=wl.num_pages,
                     page_size=wl.page_size, max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads,
-                    idx_dim=wl.idx_dim, idx_dtype=dsa.DSA_FP8_E4M3 if wl.idx_fp8 else dsa.DSA_BF16,
+                    idx_dim=wl.idx_dim,
+                    idx_dtype=(dsa.DSA_MXFP8_E4M3 if wl.idx_mx else dsa.DSA_FP8_E4M3) if wl.idx_fp8 else dsa.DSA_BF16,
                     top_k=wl.top_k, attn_heads=wl.attn_heads, kv_dim=wl.kv_dim, v_dim=wl.v_dim,
                     softmax_scale=wl.softmax_scale,
                     kv_dtype=dsa.DSA_FP8_E4M3 if wl.kv_fp8 else dsa.DSA_BF16)
@@ -492,7 +496,8 @@ def run_ours(args):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("fp8-e4m3 indexer" if wl.idx_fp8 else "bf16 indexer") +
+        "dtype": (("mxfp8-e4m3 indexer (E8M0 scale per 32)" if wl.idx_mx else "fp8-e4m3 indexer") if wl.idx_fp8
+                  else "bf16 indexer") +
         (" / fp8-e4m3 latent-KV cache (128-element tile scales) dequantised to bf16 attention" if wl.kv_fp8 else
          " / bf16 attention") + ", fp32 accumulate",
         "data": "synthetic (seeded SplitMix64; N(0,1) activations, random page table)",

@@ -239,14 +239,19 @@ def config_lengths(n: int, seed: Optional[int] = None):
 
 
 def config(n: int, seed: Optional[int] = None, with_sfa: bool = True, batch: Optional[int] = None,
-           kv_fp8: bool = False) -> Workload:
+           kv_fp8: bool = False, idx_mx: bool = False) -> Workload:
     """Workload of configuration n (1..5).  `batch` truncates to the first sequences (same data);
-    `kv_fp8` stores the latent-KV cache in the FP8 layout (same bf16 rows, quantised)."""
+    `kv_fp8` stores the latent-KV cache in the FP8 layout (same bf16 rows, quantised); `idx_mx` makes
+    the indexer inputs MXFP8 (the same bf16 rows with one E8M0 scale per 32 elements)."""
     seed = 1000 + n if seed is None else seed
     lens, qls = config_lengths(n, seed)
     if batch is not None:
         lens, qls = lens[:batch], qls[:batch]
     common = dict(with_sfa=with_sfa, kv_fp8=kv_fp8)
+    if idx_mx:
+        return make_workload(CONFIG_NAMES[n] + "_mxfp8", seed, lens, qls, idx_heads=64, idx_dim=128, idx_fp8=True,
+                             idx_mx=True, top_k=2048, attn_heads=128, w_hi=0.125,
+                             salient_frac=0.01 if n in (2, 3) else 0.0, **common)
     if n == 1:
         return make_workload(CONFIG_NAMES[1], seed, lens, qls, idx_heads=4, idx_dim=64, idx_fp8=False, top_k=256,
                              attn_heads=16, w_hi=1.0, **common)

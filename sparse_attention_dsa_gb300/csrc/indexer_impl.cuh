@@ -601,7 +601,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     uint32_t* keys = reinterpret_cast<uint32_t*>(q_tile + Cfg::kQBytes);  // QB * chunk
     float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
     float* qf_s = w_s + Cfg::kN;  // MX: 2^(e - 127) of every (head, group) query scale, [kN][kGroups]
-    int32_t* pages_s = reinterpret_cast<int32_t*>(qf_s + (MX ? Cfg::kN * Cfg::kGroups : 0));  // chunk / 64, padded
+    // MX: the second half of the epilogue warps hands its per-position partial sums to the first through
+    // xch_s ([2 tiles][128 positions]), one mbarrier per (tile parity, TMEM lane quadrant)
+    float* xch_s = qf_s + (MX ? Cfg::kN * Cfg::kGroups : 0);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(xch_s + (MX ? 2 * kTileM : 0));
+    int32_t* pages_s = reinterpret_cast<int32_t*>(xbar + (MX ? 8 : 0));  // chunk / 64, padded
     // everything after the page list is read with 16-byte vector loads: keep it 16-byte aligned
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + page_words(p.chunk));  // QB x 256
     uint32_t* allh = hist0 + QB * 256;                                      // C x 768 (select exchange)
@@ -681,9 +685,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
-            mbar_init(&ctl->tempty[i], 4);
+            mbar_init(&ctl->tempty[i], MX ? 8 : 4);  // one arrival per epilogue warp
         }
         mbar_init(&ctl->qbar, 1);
+        if (MX)
+            for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 1);  // one arrival: the partner warp's lane 0
         ctl->consumed = 0;
         ctl->issued = 0;
         ctl->qwaited = 0;
@@ -777,9 +783,12 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 __syncwarp();
             }
             if (lane == 0) ctl->consumed = consumed;
-        } else if (warp >= 2 && warp < 6) {
+        } else if (warp >= 2 && warp < (MX ? 10 : 6)) {
+            // (MX: eight epilogue warps, two per TMEM lane quadrant, each taking half of the heads)
+            static_assert(!MX || NT >= 320, "the MX epilogue uses warps 2-9");
             const uint32_t quad = (uint32_t)(warp & 3);  // TMEM lanes this warp may access
             const int row = (int)quad * 32 + lane;       // position within the tile
+            const int half = MX ? (warp - 2) >> 2 : 0;
             const uint32_t tmem = ctl->tmem_base + ((quad * 32u) << 16);
             int64_t pq[QB];
 #pragma unroll
@@ -808,7 +817,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     for (int g = 0; g < 4; ++g) f[g] = e8m0_factor((kexp >> (8 * g)) & 255u);
                     float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                    for (int c0 = 0; c0 < HI; c0 += 16) {
+                    for (int c0 = half * (HI / 2); c0 < (half + 1) * (HI / 2); c0 += 16) {
                         float v[4][16];
 #pragma unroll
                         for (int g = 0; g < 4; ++g) tmem_ld16(tmem + ab * Cfg::kAccCols + g * Cfg::kN + c0, v[g]);
@@ -826,6 +835,21 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                         }
                     }
                     acc[0] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                    // the second half's sums go to the first half of the same quadrant; the first half reads
+                    // them before it releases the accumulators, so a slot is never overwritten early
+                    float* slot = xch_s + (i & 1) * kTileM + row;
+                    uint64_t* xb = &xbar[(i & 1) * 4 + quad];
+                    if (half == 1) {
+                        *slot = acc[0];
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(xb);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctl->tempty[ab]);
+                        continue;
+                    }
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(xb, ((uint32_t)i >> 1) & 1u, p.err))) break;
+                    acc[0] += *slot;
                 } else if constexpr (HI % 32 == 0) {
                     // One query's heads, 32 columns per TMEM wait, in a rolled loop: the code stays small
                     // (it shares the instruction cache with the MMA warp), eight independent partial sums
@@ -926,6 +950,8 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             mbar_inval(&ctl->tempty[i]);
         }
         mbar_inval(&ctl->qbar);
+        if (MX)
+            for (int i = 0; i < 8; ++i) mbar_inval(&xbar[i]);
     }
 }
 
@@ -933,7 +959,7 @@ template <int HI, int DI, int QB, bool FP8, bool MX = false>
 size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
     using Cfg = IdxCfg<HI, DI, QB, FP8, MX>;
     return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
-           (MX ? (size_t)Cfg::kN * Cfg::kGroups * 4 : 0) +
+           (MX ? (size_t)Cfg::kN * Cfg::kGroups * 4 + 2 * kTileM * 4 + 8 * 8 : 0) +
            (size_t)page_words(chunk) * 4 + (size_t)(QB + 3 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
            64;
 }
