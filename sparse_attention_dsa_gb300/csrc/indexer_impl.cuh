@@ -399,25 +399,35 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     for (uint32_t r = 0; r < C; ++r) n_c += S.ncand_in[r];
     uint32_t T;
     if (fits && n_c <= (uint32_t)kRankPick) {
-        // Every CTA holds the same few candidates: the remaining-th largest of them is the K-th key.  A
-        // thread per candidate counts the candidates above and equal to its own.
+        // Every CTA holds the same few candidates: the remaining-th largest of them is the K-th key.  They
+        // are flattened into the idle stage ring first; then a group of `subs` lanes per candidate splits
+        // the count of the candidates above and equal to its own, and sums it with shuffles.
         __syncthreads();
         for (uint32_t c = (uint32_t)tid; c < n_c; c += NT) {
             uint32_t r = 0, j = c;
             while (j >= S.ncand_in[r]) j -= S.ncand_in[r++];
-            const uint32_t key = cand[r * kCandCap + j];
+            sbuf[c] = cand[r * kCandCap + j];
+        }
+        __syncthreads();
+        const uint32_t subs = n_c * 8 <= (uint32_t)NT ? 8u : n_c * 4 <= (uint32_t)NT ? 4u : n_c * 2 <= (uint32_t)NT ? 2u : 1u;
+        for (uint32_t base = 0; base < n_c * subs; base += NT) {  // the same trip count in every thread
+            const uint32_t idx = base + (uint32_t)tid, c = idx / subs, sb = idx % subs;
+            const bool valid = c < n_c;
+            const uint32_t key = valid ? sbuf[c] : 0u;
             uint32_t above = 0, equal = 0;
-            for (uint32_t r2 = 0; r2 < C; ++r2) {
-                const uint32_t* cr = cand + r2 * kCandCap;
-                const uint32_t m = S.ncand_in[r2];
+            if (valid) {
 #pragma unroll 4
-                for (uint32_t j2 = 0; j2 < m; ++j2) {
-                    const uint32_t k2 = cr[j2];
+                for (uint32_t j = sb; j < n_c; j += subs) {
+                    const uint32_t k2 = sbuf[j];
                     above += k2 > key ? 1u : 0u;
                     equal += k2 == key ? 1u : 0u;
                 }
             }
-            if (above < remaining && remaining <= above + equal) {  // every equal candidate writes the same
+            for (uint32_t off = 1; off < subs; off <<= 1) {  // the group's lanes are consecutive within a warp
+                above += __shfl_xor_sync(0xFFFFFFFFu, above, off);
+                equal += __shfl_xor_sync(0xFFFFFFFFu, equal, off);
+            }
+            if (valid && sb == 0 && above < remaining && remaining <= above + equal) {  // all equal keys agree
                 S.res[0] = key;
                 S.res[1] = remaining - above;
             }
