@@ -684,7 +684,63 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             const int quad = warp & 3, part = (warp - 2) >> 2;  // part 0..2 within the quadrant
             const int hh = quad * 32 + lane, r = hh - ps * slice;
             const bool own_row = r >= 0 && r < rows_here;
-            if (__any_sync(0xFFFFFFFFu, own_row)) {
+            if (P == 2 && __any_sync(0xFFFFFFFFu, own_row)) {
+                // the common case, two splits: the same arithmetic as below with one other split, in compact
+                // code (this runs once per launch)
+                const uint32_t tr = tmem + (((uint32_t)quad * 32u) << 16);
+                const int jo = 1 - ps;
+                float2 mo = make_float2(-INFINITY, 0.f), mt = make_float2(-INFINITY, 0.f);
+                if (own_row) {
+                    const float* base = p.merge + kSfaMergeRows * 256;
+                    mo = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(cta0 + 2 * ps) * kSfaMergeFloatsPerCta) + hh);
+                    mt = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(cta0 + 2 * jo) * kSfaMergeFloatsPerCta) + hh);
+                }
+                float M = -INFINITY;
+                if (mo.y > 0.f) M = fmaxf(M, mo.x);
+                if (mt.y > 0.f) M = fmaxf(M, mt.x);
+                float w_own = mo.y > 0.f ? exp2f(mo.x - M) : 0.f, w_oth = mt.y > 0.f ? exp2f(mt.x - M) : 0.f;
+                const float Lsum = mo.y * w_own + mt.y * w_oth;
+                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+                w_own *= inv;
+                w_oth *= inv;
+                if (part == 0 && own_row && dvh == 0 && p.lse)
+                    p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+                const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->merge_full, 0, p.err));
+                const int c_lo = part == 0 ? 0 : (part == 1 ? 6 : 11), c_hi = part == 0 ? 6 : (part == 1 ? 11 : 16);
+                const uint32_t rowp = smem_u32(obuf) + (uint32_t)(jo * slice + r) * 1024u;
+#pragma unroll 1
+                for (int c = c_lo; c < c_hi; ++c) {
+                    float o[16];
+                    tmem_ld16(tr + c * 16, o);
+                    tmem_ld_wait();
+                    tmem_regs_ready(o);
+                    if (own_row && got) {
+                        // a split with no selected row has weight 0 and an O that is never read: select, not scale
+                        float acc[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) acc[k] = w_own != 0.f ? o[k] * w_own : 0.f;
+                        if (w_oth != 0.f) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                float4 v;
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                             : "r"(rowp + (((c * 4 + k) ^ (r & 7)) << 4)));
+                                acc[4 * k] += v.x * w_oth;
+                                acc[4 * k + 1] += v.y * w_oth;
+                                acc[4 * k + 2] += v.z * w_oth;
+                                acc[4 * k + 3] += v.w * w_oth;
+                            }
+                        }
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) pk[k] = f2_to_bf2(acc[2 * k], acc[2 * k + 1]);
+                        uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)t * p.heads + hh) * kVDim + dvh * kOCols + c * 16);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+            } else if (__any_sync(0xFFFFFFFFu, own_row)) {
                 const uint32_t tr = tmem + (((uint32_t)quad * 32u) << 16);
                 // weights of the splits for this row: exp2(m_j - M) / sum_j l_j exp2(m_j - M)
                 float2 ml[kMaxSplits];

@@ -37,6 +37,8 @@ SMALL = {
     "hi64_fp8": ([5000, 190, 1], [1, 2, 1], 64, 128, True, 256, 128, {}),
     "hi64_salient": ([4100, 8192], [1, 1], 64, 128, False, 2048, 128, dict(w_hi=0.125, salient_frac=0.01)),
     "k_equals_one": ([700, 64], [1, 1], 64, 128, False, 1, 32, {}),
+    # 32 query tokens: the attention splits each token's positions in two (the two-split merge path)
+    "thirty_two_tokens": ([700 + 97 * i for i in range(32)], [1] * 32, 64, 128, False, 512, 128, {}),
 }
 
 
