@@ -116,6 +116,7 @@ cudaError_t launch_decode_variant(const IndexerLaunch& IL, const SfaLaunch& SL, 
     ip.stages = d.stages;
     SfaParams sp = SL.params;
     sp.splits = d.P;
+    sp.one_query_per_seq = 1;  // decode_shape_ok: every sequence has exactly one query token
     sp.early_setup = 0;
     return cudaLaunchKernelEx(&cfg, kern, IL.kmap, IL.qmap, ip, SL.qmap, sp);
 }

@@ -76,6 +76,7 @@ struct SfaParams {
     float* merge;         // split-merge scratch: sfa_merge_floats_per_cta() floats per CTA of the grid
     int32_t kv_fp8;       // kv_cache rows are in the FP8 row layout
     const int32_t* rows_in;  // [T, K] physical rows of topk written by the indexer phase in the same launch, or null
+    int32_t one_query_per_seq;  // every sequence has exactly one query token: token t belongs to sequence t
 };
 
 struct SfaLaunch {

@@ -196,26 +196,40 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         }
     };
     if (!p.early_setup) load_entries();  // overlaps the sequence search
-    // the sequence that holds token t: a parallel search over the query offsets
-    if (tid == 0) ctl->tok_b = -1;
-    __syncthreads();
-    for (int j = tid; j < p.batch; j += kThreadsSfa) {
-        const int c0 = __ldg(p.cu_q_lens + j), c1 = __ldg(p.cu_q_lens + j + 1);
-        if (c0 <= t && t < c1) {  // one sequence when the offsets are non-decreasing
-            ctl->tok_b = j;
-            ctl->tok_cu0 = c0;
-            ctl->tok_cu1 = c1;
+    // the sequence that holds token t: a parallel search over the query offsets, or (one query token per
+    // sequence) sequence t, whose offsets and length are then loaded together and checked
+    int b, cu0, cu1, L;
+    if (p.one_query_per_seq) {
+        b = t;
+        cu0 = __ldg(p.cu_q_lens + t);
+        cu1 = __ldg(p.cu_q_lens + t + 1);
+        L = __ldg(p.seq_lens + t);
+        if (cu0 != t || cu1 != t + 1) {
+            if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
+            return;  // uniform over the cluster (same token)
         }
+    } else {
+        if (tid == 0) ctl->tok_b = -1;
+        __syncthreads();
+        for (int j = tid; j < p.batch; j += kThreadsSfa) {
+            const int c0 = __ldg(p.cu_q_lens + j), c1 = __ldg(p.cu_q_lens + j + 1);
+            if (c0 <= t && t < c1) {  // one sequence when the offsets are non-decreasing
+                ctl->tok_b = j;
+                ctl->tok_cu0 = c0;
+                ctl->tok_cu1 = c1;
+            }
+        }
+        __syncthreads();
+        b = ctl->tok_b;
+        if (b < 0) {
+            if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
+            return;  // uniform over the cluster (same token)
+        }
+        cu0 = ctl->tok_cu0;
+        cu1 = ctl->tok_cu1;
+        L = __ldg(p.seq_lens + b);
     }
-    __syncthreads();
-    const int b = ctl->tok_b;
-    if (b < 0) {
-        if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
-        return;  // uniform over the cluster (same token)
-    }
-    const int cu0 = ctl->tok_cu0, cu1 = ctl->tok_cu1;
     const int n_b = cu1 - cu0;
-    const int L = __ldg(p.seq_lens + b);
     if (n_b > L || L > p.max_pages * 64) {
         if (tid == 0 && dvh == 0 && ps == 0) raise_error(p.err, DSA_DEVERR_SEQ);
         return;  // uniform over the cluster (same token)
