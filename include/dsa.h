@@ -63,7 +63,9 @@ typedef enum {
                            ([A3] 3.1); latent-KV rows in the FP8 row layout below */
     DSA_MXFP8_E4M3 = 2  /* indexer only: E4M3 codes with one E8M0 scale byte per 32 consecutive elements
                            of a row (OCP MX: the byte e means 2^(e - 127); [A1] 1, [A4] 4.1 "MXFP8,
-                           per-group 32") */
+                           per-group 32").  The NaN codes 0x7F and 0xFF, which a saturating encoder
+                           never writes, are not propagated from k_cache (the kernel reads them as
+                           +-480 times the scale); a scale byte of 255 (NaN) is. */
 } dsa_dtype_t;
 
 /*

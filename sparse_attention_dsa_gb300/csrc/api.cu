@@ -253,6 +253,7 @@ dsa_status_t prepare_indexer(const dsa_dims_t* d, const void* q_idx, const float
     if ((st = encode_indexer_maps(d, q_idx, k_cache, n_cols, &L))) return st;
     dsa::IndexerParams& p = L.params;
     p.q_scale = fp8 ? q_scale : nullptr;
+    p.q_idx_codes = L.mx ? q_idx : nullptr;
     p.w = w;
     p.k_scale = fp8 ? k_scale : nullptr;
     p.page_table = page_table;

@@ -26,8 +26,11 @@ cudaError_t launch_variant(const IndexerLaunch& L, cudaStream_t stream) {
     // choose the number of pipeline stages from the shared-memory budget
     int stages = kMaxStages;
     while (stages > 2 && indexer_smem_bytes<HI, DI, QB, FP8, MX>(stages, chunk, L.cluster) > (size_t)L.smem_limit) --stages;
-    const size_t smem = indexer_smem_bytes<HI, DI, QB, FP8, MX>(stages, chunk, L.cluster);
+    size_t smem = indexer_smem_bytes<HI, DI, QB, FP8, MX>(stages, chunk, L.cluster);
     if (smem > (size_t)L.smem_limit) return cudaErrorInvalidConfiguration;
+    // a CTA that takes all of TMEM must be alone on its SM (a second one would wait in its allocation
+    // for a cluster peer that waits for it): more than half the shared memory keeps it alone
+    if (IdxCfg<HI, DI, QB, FP8, MX>::kTmemCols == 512 && 2 * smem <= (size_t)L.smem_limit) smem = L.smem_limit / 2 + 1024;
     IndexerParams prm = L.params;
     prm.stages = stages;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

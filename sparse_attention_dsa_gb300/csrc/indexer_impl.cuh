@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -42,28 +44,36 @@ constexpr int kTileM = 128;  // positions per tile (two pages)
 constexpr int kPage = 64;
 constexpr int kMaxCluster = 16;
 
-// MX: FP8 with one E8M0 scale per 32 elements of a row (MXFP8): every 32-element K step gets its own
-// accumulator, and the epilogue applies the two groups' scales before the ReLU.
+// MX: FP8 codes with one E8M0 scale per 32 elements of a row (MXFP8).  A code times its group's power of
+// two is exact in bf16, so the K tiles are dequantised to bf16 by converter warps (the query once at
+// set-up) and scored by the bf16 MMA: one accumulator, and the epilogue of the other variants.
 template <int HI, int DI, int QB, bool FP8, bool MX = false>
 struct IdxCfg {
-    static_assert(!MX || (FP8 && QB == 1 && DI % 32 == 0), "MXFP8: FP8 codes, one query per work item");
+    static_assert(!MX || (FP8 && QB == 1 && DI == 128), "MXFP8: FP8 codes of 128 dims, one query per work item");
     static constexpr int kNReal = HI * QB;
     static constexpr int kN = kNReal < 16 ? 16 : ((kNReal + 15) / 16) * 16;  // UMMA N for M = 128
-    static constexpr int kGroups = MX ? DI / 32 : 1;     // accumulators per tile (scale groups along K)
-    static constexpr int kAccCols = kN * kGroups;        // TMEM columns of one tile's accumulators
-    static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr int kAccCols = kN;                  // TMEM columns of one tile's accumulator
+    static constexpr int kElem = FP8 ? 1 : 2;            // bytes per element of the cached K tiles
     static constexpr int kRowBytes = DI * kElem;
-    static constexpr int kAtoms = kRowBytes / 128;  // 128-byte swizzle atoms along K
+    static constexpr int kAtoms = kRowBytes / 128;  // 128-byte swizzle atoms along K (of the loaded tiles)
     static constexpr int kStageBytes = kTileM * kRowBytes;
-    static constexpr int kQBytes = kN * kRowBytes;
-    static constexpr int kMmaK = FP8 ? 32 : 16;  // elements per UMMA
+    static constexpr bool kMmaBf16 = !FP8 || MX;         // the MMA reads bf16 tiles
+    static constexpr int kMmaElem = kMmaBf16 ? 2 : 1;
+    static constexpr int kQBytes = kN * DI * kMmaElem;   // the query tile as the MMA reads it
+    static constexpr int kScaleStageBytes = MX ? kTileM * (DI / 32) : 0;  // a tile's E8M0 key scales (MX)
+    static constexpr int kMmaK = kMmaBf16 ? 16 : 32;  // elements per UMMA
     static constexpr int kKSteps = DI / kMmaK;
     // accumulator buffers in TMEM: enough that the MMA issuer rarely waits for the epilogue
     static constexpr int kAccBufs = (4 * kAccCols) <= 512 ? 4 : 2;
-    static constexpr int kTmemCols = (kAccBufs * kAccCols) <= 32 ? 32 : (kAccBufs * kAccCols) <= 64 ? 64
-                                     : (kAccBufs * kAccCols) <= 128 ? 128 : (kAccBufs * kAccCols) <= 256 ? 256 : 512;
-    static_assert(kAccBufs * kAccCols <= 512, "TMEM columns");
-    static constexpr uint32_t kIdesc = make_idesc(128, kN, FP8 ? 0u : 1u, FP8 ? 0u : 1u, 0u, 0u);
+    // MX: two dequantised K tiles in TMEM after the accumulators (the MMA's A operand; lane = key row,
+    // column j = dims 2j and 2j + 1 as a bf16 pair)
+    static constexpr int kACol = kAccBufs * kAccCols;
+    static constexpr int kACols = MX ? DI / 2 : 0;
+    static constexpr int kUsedCols = kACol + 2 * kACols;
+    static constexpr int kTmemCols = kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128
+                                     : kUsedCols <= 256 ? 256 : 512;
+    static_assert(kUsedCols <= 512, "TMEM columns");
+    static constexpr uint32_t kIdesc = make_idesc(128, kN, kMmaBf16 ? 1u : 0u, kMmaBf16 ? 1u : 0u, 0u, 0u);
     static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
     // the select's fallback exchange space (2 x C x 256 words) lives in the stage ring (at least 2 stages)
     static_assert(2 * kStageBytes >= 2 * kMaxCluster * 256 * 4, "stage ring too small for the select");
@@ -99,12 +109,47 @@ struct CtrlSmem {
     uint64_t empty[kMaxStages];
     uint64_t tfull[4];
     uint64_t tempty[4];
+    uint64_t bfull[2];   // MX: a dequantised K tile is ready (converter warps)
+    uint64_t bempty[2];  // MX: its MMAs are done
     uint64_t qbar;
     uint32_t tmem_base;
     int32_t consumed;  // tiles consumed by the MMA warp (drain bookkeeping)
     int32_t issued;    // tiles issued by the producer
     int32_t qwaited;
 };
+
+// MX key dequantisation without conversion instructions.  An E4M3 code c placed in a bf16 as
+// (c & 0x80) << 8 | (c & 0x7F) << 4 (its exponent field in the low four exponent bits, its mantissa in
+// the top three mantissa bits) is exactly 2^-120 times the code's value, subnormal codes included
+// (they land on bf16 subnormals with the same spacing); the group scale 2^(e - 127) then makes it a
+// product by 2^(e - 7), exact in bf16 for every finite result.  Returns the bf16x2 word of the codes
+// in bytes b0 and b1 of w (b0 in the low half): a byte permute (sel = 0x1804 for bytes 0 and 1, 0x3A24
+// for bytes 2 and 3) builds [b1 | sign(b0) x 8 | b0 | 0], and one arithmetic shift by four then leaves
+// each code's sign at its half's bit 15 and its low seven bits at bits 4..10; the mask clears the
+// sign copies in between.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_unscaled(uint32_t w, uint32_t sel) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w), "r"(0u), "r"(sel));
+    return (uint32_t)((int32_t)t >> 4) & 0x87F087F0u;
+}
+
+// bf16x2 a * b, nearest-even, subnormals kept (as a fused multiply-add with -0)
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0x80008000u));
+    return d;
+}
+
+// The factor 2^(e - 7) of E8M0 byte e as a bf16x2 pair, split in two when it exceeds the bf16 range:
+// lo = 2^min(e - 7, 127) (NaN for e = 255), hi = 2^max(e - 134, 0).
+__device__ __forceinline__ uint32_t mx_factor_lo(uint32_t e) {
+    const uint32_t b = e == 255u ? 0x7FC0u : (min(e + 120u, 254u) << 7);
+    return b | (b << 16);
+}
+__device__ __forceinline__ uint32_t mx_factor_hi(uint32_t e) {
+    const uint32_t b = (max(e, 134u) - 7u) << 7;
+    return b | (b << 16);
+}
 
 // E8M0 scale byte e as the float 2^(e - 127) (e = 0: 2^-127, a subnormal; e = 255: NaN).
 __device__ __forceinline__ float e8m0_factor(uint32_t e) {
@@ -608,14 +653,10 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     const int S = p.stages;
     uint8_t* a_tiles = smem;                                   // S * kStageBytes
     uint8_t* q_tile = a_tiles + (size_t)S * Cfg::kStageBytes;  // kQBytes
-    uint32_t* keys = reinterpret_cast<uint32_t*>(q_tile + Cfg::kQBytes);  // QB * chunk
+    uint8_t* kexp_ring = q_tile + Cfg::kQBytes;                // MX: S * kScaleStageBytes, beside the stages
+    uint32_t* keys = reinterpret_cast<uint32_t*>(kexp_ring + (size_t)S * Cfg::kScaleStageBytes);  // QB * chunk
     float* w_s = reinterpret_cast<float*>(keys + (size_t)QB * p.chunk);   // kN
-    float* qf_s = w_s + Cfg::kN;  // MX: 2^(e - 127) of every (head, group) query scale, [kN][kGroups]
-    // MX: the second half of the epilogue warps hands its per-position partial sums to the first through
-    // xch_s ([2 tiles][128 positions]), one mbarrier per (tile parity, TMEM lane quadrant)
-    float* xch_s = qf_s + (MX ? Cfg::kN * Cfg::kGroups : 0);
-    uint64_t* xbar = reinterpret_cast<uint64_t*>(xch_s + (MX ? 2 * kTileM : 0));
-    int32_t* pages_s = reinterpret_cast<int32_t*>(xbar + (MX ? 8 : 0));  // chunk / 64, padded
+    int32_t* pages_s = reinterpret_cast<int32_t*>(w_s + Cfg::kN);         // chunk / 64, padded to 16 bytes
     // everything after the page list is read with 16-byte vector loads: keep it 16-byte aligned
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(pages_s + page_words(p.chunk));  // QB x 256
     uint32_t* allh = hist0 + QB * 256;                                      // C x 768 (select exchange)
@@ -681,25 +722,37 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         w_s[c] = wv;
     }
     if constexpr (MX) {
-        // the query's scale bytes [T, Hi, kGroups] as factors 2^(e - 127)
+        // the query tile dequantised to bf16 (exact: a code times a power of two) in the MMA's swizzled
+        // K-major layout: head row h, 16-byte chunk j (dims 8j..8j+7) of atom j / 8
+        const uint8_t* qc = reinterpret_cast<const uint8_t*>(p.q_idx_codes);
         const uint8_t* qe = reinterpret_cast<const uint8_t*>(p.q_scale);
-        for (int i = tid; i < Cfg::kN * Cfg::kGroups; i += NT) {
-            const int c = i / Cfg::kGroups, g = i % Cfg::kGroups;
-            qf_s[i] = c < nq * HI ? e8m0_factor(qe[((int64_t)t0 * HI + c) * Cfg::kGroups + g]) : 0.f;
+        const uint32_t qb = smem_u32(q_tile);
+        for (int i = tid; i < Cfg::kN * (DI / 8); i += NT) {
+            const int h = i / (DI / 8), j = i % (DI / 8);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (h < nq * HI) {
+                const int64_t qrow = (int64_t)t0 * HI + h;
+                const uint2 codes = __ldg(reinterpret_cast<const uint2*>(qc + qrow * DI + 8 * j));
+                v = e4m3x8_to_bf16x8(codes, e8m0_factor(__ldg(qe + qrow * (DI / 32) + j / 4)));
+            }
+            st_shared_v4(qb + (j / 8) * (Cfg::kN * 128) + h * 128 + (((j % 8) ^ (h & 7)) << 4), v);
         }
+        fence_proxy_async_smem();  // read by the MMAs through the async proxy
     }
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->empty[s], MX ? 4 : 1);  // MX: the four converter warps free the stage
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
-            mbar_init(&ctl->tempty[i], MX ? 8 : 4);  // one arrival per epilogue warp
+            mbar_init(&ctl->tempty[i], 4);  // one arrival per epilogue warp
         }
         mbar_init(&ctl->qbar, 1);
-        if (MX)
-            for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 1);  // one arrival: the partner warp's lane 0
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl->bfull[i], 4);  // MX: one arrival per converter warp
+            mbar_init(&ctl->bempty[i], 1);
+        }
         ctl->consumed = 0;
         ctl->issued = 0;
         ctl->qwaited = 0;
@@ -712,6 +765,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (MX && tid == 0) mbar_arrive(&ctl->qbar);  // the dequantised query tile is in place
 
     // ---- scoring pipeline -----------------------------------------------------------------------------
     if (ntiles > 0) {
@@ -720,11 +774,13 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         if (warp == 0) {
             if (lane == 0) {
                 prefetch_tensormap(&kmap);
-                prefetch_tensormap(&qmap);
-                mbar_arrive_expect_tx(&ctl->qbar, Cfg::kQBytes);
+                if (!MX) {
+                    prefetch_tensormap(&qmap);
+                    mbar_arrive_expect_tx(&ctl->qbar, Cfg::kQBytes);
 #pragma unroll
-                for (int a = 0; a < Cfg::kAtoms; ++a)
-                    tma_load_2d(q_tile + a * Cfg::kN * 128, &qmap, &ctl->qbar, a * (128 / Cfg::kElem), t0 * HI);
+                    for (int a = 0; a < Cfg::kAtoms; ++a)
+                        tma_load_2d(q_tile + a * Cfg::kN * 128, &qmap, &ctl->qbar, a * (128 / Cfg::kElem), t0 * HI);
+                }
             }
             int issued = 0;
             // the K cache is read once per step: evict-first, so its stream does not push the kernel's code
@@ -736,7 +792,8 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->empty[s], ph ^ 1u, p.err))) break;
                 if (lane == 0) {
                     const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
-                    const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * (kPage * Cfg::kRowBytes);
+                    const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) *
+                                           (kPage * Cfg::kRowBytes + Cfg::kScaleStageBytes / 2);
                     if (bytes == 0) {
                         mbar_arrive(&ctl->full[s]);
                     } else {
@@ -750,6 +807,16 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                             if (pg1 >= 0)
                                 tma_load_3d_hint(dst + a * (kTileM * 128) + kPage * 128, &kmap, &ctl->full[s],
                                                  a * (128 / Cfg::kElem), 0, pg1, kpol);
+                        }
+                        if (MX) {  // each page's 64 x 4 scale bytes, contiguous in the cache
+                            constexpr uint32_t kPageScaleBytes = Cfg::kScaleStageBytes / 2;
+                            uint8_t* sdst = kexp_ring + (size_t)s * Cfg::kScaleStageBytes;
+                            const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(p.k_scale);
+                            if (pg0 >= 0)
+                                bulk_copy_g2s(sdst, ssrc + (int64_t)pg0 * kPageScaleBytes, kPageScaleBytes, &ctl->full[s]);
+                            if (pg1 >= 0)
+                                bulk_copy_g2s(sdst + kPageScaleBytes, ssrc + (int64_t)pg1 * kPageScaleBytes,
+                                              kPageScaleBytes, &ctl->full[s]);
                         }
                     }
                 }
@@ -769,36 +836,105 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 const int ab = i % Cfg::kAccBufs;
                 const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err))) break;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->full[s], ph, p.err))) break;
+                // the tile to score: the loaded stage, or (MX) its dequantised copy in TMEM
+                uint64_t* ready = MX ? &ctl->bfull[i & 1] : &ctl->full[s];
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err))) break;
                 consumed = i + 1;
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t a_base = smem_u32(a_tiles + (size_t)s * Cfg::kStageBytes);
 #pragma unroll
                     for (int k = 0; k < Cfg::kKSteps; ++k) {
-                        const int kb = k * Cfg::kMmaK * Cfg::kElem;  // byte offset along K
+                        const int kb = k * Cfg::kMmaK * Cfg::kMmaElem;  // byte offset along K
                         const int atom = kb / 128, off = kb % 128;
                         const uint64_t ad = smem_desc(a_base + atom * (kTileM * 128) + off, 16, 1024, kSwizzle128B);
                         const uint64_t bd = smem_desc(q_base + atom * (Cfg::kN * 128) + off, 16, 1024, kSwizzle128B);
-                        if (MX)  // one 32-element scale group per K step: its own accumulator
-                            umma_f8_ss(tmem + ab * Cfg::kAccCols + k * Cfg::kN, ad, bd, Cfg::kIdesc, 0u);
-                        else if (FP8)
-                            umma_f8_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
-                        else
+                        if (MX)
+                            umma_f16_ts(tmem + ab * Cfg::kN, tmem + Cfg::kACol + (i & 1) * Cfg::kACols + k * 8, bd,
+                                        Cfg::kIdesc, k > 0);
+                        else if (Cfg::kMmaBf16)
                             umma_f16_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
+                        else
+                            umma_f8_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
                     }
-                    umma_commit(&ctl->empty[s]);
+                    umma_commit(MX ? &ctl->bempty[i & 1] : &ctl->empty[s]);
                     umma_commit(&ctl->tfull[ab]);
                 }
                 __syncwarp();
             }
-            if (lane == 0) ctl->consumed = consumed;
-        } else if (warp >= 2 && warp < (MX ? 10 : 6)) {
-            // (MX: eight epilogue warps, two per TMEM lane quadrant, each taking half of the heads)
-            static_assert(!MX || NT >= 320, "the MX epilogue uses warps 2-9");
+            if (lane == 0 && !MX) ctl->consumed = consumed;
+        } else if (MX && warp >= 6 && warp < 10) {
+            // MX converters: each landed FP8 tile, dequantised to bf16 with the key's group scales, goes to
+            // one of two TMEM tiles the MMA reads as its A operand; the FP8 stage is then free again
+            static_assert(NT >= 320, "the MX converters are warps 6-9");
+            const int row = (warp & 3) * 32 + lane;  // position within the tile = the TMEM lane this warp may write
+            const uint32_t trow = ctl->tmem_base + (((uint32_t)(warp & 3) * 32u) << 16) + Cfg::kACol;
+            int consumed = 0, s = 0;
+            uint32_t ph = 0;
+            // half a row: chunks h*4 .. h*4+3 of 16 codes (chunk c: dims 16c..16c+15, scale group c / 2)
+            // times their group factors, stored as TMEM columns 32h .. 32h+31 of the row; BIG: factors
+            // beyond 2^127 take a second product
+            auto convert = [&](auto big_tag, int h, uint32_t kexp, uint32_t src, uint32_t dst) {
+                constexpr bool BIG = decltype(big_tag)::value;
+                uint4 in[4];
+                uint32_t o[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(in[j].x), "=r"(in[j].y), "=r"(in[j].z), "=r"(in[j].w)
+                                 : "r"(src + (((4 * h + j) ^ (row & 7)) << 4)));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = 4 * h + j;
+                    const uint32_t e = (kexp >> (8 * (c / 2))) & 255u;
+                    const uint32_t flo = mx_factor_lo(e);
+                    const uint32_t fhi = BIG ? mx_factor_hi(e) : 0u;
+                    const uint32_t wd[4] = {in[j].x, in[j].y, in[j].z, in[j].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t& lo = o[8 * j + 2 * k];
+                        uint32_t& hi = o[8 * j + 2 * k + 1];
+                        lo = bf16x2_mul(e4m3x2_to_bf16x2_unscaled(wd[k], 0x1804u), flo);
+                        hi = bf16x2_mul(e4m3x2_to_bf16x2_unscaled(wd[k], 0x3A24u), flo);
+                        if (BIG) {
+                            lo = bf16x2_mul(lo, fhi);
+                            hi = bf16x2_mul(hi, fhi);
+                        }
+                    }
+                }
+                tmem_st16_u32(dst + 32 * h, o);
+                tmem_st16_u32(dst + 32 * h + 16, o + 16);
+            };
+            for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->full[s], ph, p.err))) break;
+                consumed = i + 1;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->bempty[i & 1], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+                tc_fence_after();  // the MMAs that read this TMEM tile have completed
+                const uint32_t src = smem_u32(a_tiles + (size_t)s * Cfg::kStageBytes) + row * 128;
+                const uint32_t dst = trow + (uint32_t)((i & 1) * Cfg::kACols);
+                uint32_t kexp;  // the row's four scale bytes (group g in byte g)
+                asm volatile("ld.shared.b32 %0, [%1];"
+                             : "=r"(kexp)
+                             : "r"(smem_u32(kexp_ring + (size_t)s * Cfg::kScaleStageBytes) + row * 4));
+                if (__any_sync(0xFFFFFFFFu, __vcmpgtu4(kexp, 0x86868686u) != 0u)) {
+                    convert(std::true_type{}, 0, kexp, src, dst);
+                    convert(std::true_type{}, 1, kexp, src, dst);
+                } else {
+                    convert(std::false_type{}, 0, kexp, src, dst);
+                    convert(std::false_type{}, 1, kexp, src, dst);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ctl->empty[s]);
+                    mbar_arrive(&ctl->bfull[i & 1]);
+                }
+            }
+            if (lane == 0 && warp == 6) ctl->consumed = consumed;
+        } else if (warp >= 2 && warp < 6) {
             const uint32_t quad = (uint32_t)(warp & 3);  // TMEM lanes this warp may access
             const int row = (int)quad * 32 + lane;       // position within the tile
-            const int half = MX ? (warp - 2) >> 2 : 0;
             const uint32_t tmem = ctl->tmem_base + ((quad * 32u) << 16);
             int64_t pq[QB];
 #pragma unroll
@@ -810,57 +946,13 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 const int pos = range_start + local;
                 const int32_t pg = pages_s[2 * i + (row >> 6)];
                 float ksc = 1.f;
-                uint32_t kexp = 0;  // MX: the key row's scale bytes (group g in byte g)
-                if (MX && pg >= 0) kexp = __ldg(reinterpret_cast<const uint32_t*>(p.k_scale) + (int64_t)pg * kPage + (row & 63));
-                else if (FP8 && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
+                if (FP8 && !MX && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err))) break;
                 tc_fence_after();
                 float acc[QB];
 #pragma unroll
                 for (int q = 0; q < QB; ++q) acc[q] = 0.f;
-                if constexpr (MX) {
-                    // every head's dot product is the sum over its scale groups of 2^(eq + ek) times the
-                    // group's accumulator; the ReLU and the head weight come after that sum
-                    static_assert(Cfg::kGroups == 4, "four 32-element groups per 128-dim key");
-                    float f[4];
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) f[g] = e8m0_factor((kexp >> (8 * g)) & 255u);
-                    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int c0 = half * (HI / 2); c0 < (half + 1) * (HI / 2); c0 += 16) {
-                        float v[4][16];
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + ab * Cfg::kAccCols + g * Cfg::kN + c0, v[g]);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) tmem_regs_ready(v[g]);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float4 qf = reinterpret_cast<const float4*>(qf_s)[c0 + j];
-                            float x = v[0][j] * (qf.x * f[0]);
-                            x = fmaf(v[1][j], qf.y * f[1], x);
-                            x = fmaf(v[2][j], qf.z * f[2], x);
-                            x = fmaf(v[3][j], qf.w * f[3], x);
-                            part[j & 7] = fmaf(w_s[c0 + j], fmaxf(x, 0.f), part[j & 7]);
-                        }
-                    }
-                    acc[0] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                    // the second half's sums go to the first half of the same quadrant; the first half reads
-                    // them before it releases the accumulators, so a slot is never overwritten early
-                    float* slot = xch_s + (i & 1) * kTileM + row;
-                    uint64_t* xb = &xbar[(i & 1) * 4 + quad];
-                    if (half == 1) {
-                        *slot = acc[0];
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(xb);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->tempty[ab]);
-                        continue;
-                    }
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(xb, ((uint32_t)i >> 1) & 1u, p.err))) break;
-                    acc[0] += *slot;
-                } else if constexpr (HI % 32 == 0) {
+                if constexpr (HI % 32 == 0) {
                     // One query's heads, 32 columns per TMEM wait, in a rolled loop: the code stays small
                     // (it shares the instruction cache with the MMA warp), eight independent partial sums
                     // keep the FMA chains short, and the weights come four at a time.
@@ -960,8 +1052,10 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             mbar_inval(&ctl->tempty[i]);
         }
         mbar_inval(&ctl->qbar);
-        if (MX)
-            for (int i = 0; i < 8; ++i) mbar_inval(&xbar[i]);
+        for (int i = 0; i < 2; ++i) {
+            mbar_inval(&ctl->bfull[i]);
+            mbar_inval(&ctl->bempty[i]);
+        }
     }
 }
 
@@ -969,7 +1063,7 @@ template <int HI, int DI, int QB, bool FP8, bool MX = false>
 size_t indexer_smem_bytes(int stages, int chunk, int cluster) {
     using Cfg = IdxCfg<HI, DI, QB, FP8, MX>;
     return 1024 + (size_t)stages * Cfg::kStageBytes + Cfg::kQBytes + (size_t)QB * chunk * 4 + Cfg::kN * 4 +
-           (MX ? (size_t)Cfg::kN * Cfg::kGroups * 4 + 2 * kTileM * 4 + 8 * 8 : 0) +
+           (size_t)stages * Cfg::kScaleStageBytes +
            (size_t)page_words(chunk) * 4 + (size_t)(QB + 3 * cluster) * 256 * 4 + sizeof(SelectSmem) + sizeof(CtrlSmem) +
            64;
 }

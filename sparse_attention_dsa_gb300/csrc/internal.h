@@ -29,6 +29,7 @@ struct IndexerParams {
     int32_t chunk;           // positions per CTA (multiple of 128)
     int32_t stages;          // filled in by the launcher
     int32_t* rows_out;       // [T, K] physical cache row of every selected position (-1 for padding), or null
+    const void* q_idx_codes;  // MXFP8: the q_idx codes [T, Hi, Di] (dequantised at set-up instead of loaded by TMA)
 };
 
 struct IndexerLaunch {

@@ -1,7 +1,7 @@
 """GPU parity for the MXFP8 indexer (E4M3 codes, one E8M0 scale per 32 elements of q_idx and k_idx rows):
 the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs, with the Top-K and
-attention criteria of test_gpu_parity.  The kernel keeps one tensor-core accumulator per 32-element group
-and applies 2^(eq + ek) per group before the ReLU; the oracle takes every element as code x scale."""
+attention criteria of test_gpu_parity.  The kernel dequantises both operands to bf16 (a code times a power
+of two, exact in bf16) before the tensor-core products; the oracle takes every element as code x scale."""
 import numpy as np
 import pytest
 import torch
@@ -70,3 +70,31 @@ def test_mxfp8_decode_32k_context_sampled():
     check_topk(wl, topk, [0, 4, 7])
     out, lse = dw.out_host()
     check_attention(wl, topk, out, lse, [0, 7])
+
+
+def test_mxfp8_subnormal_codes_and_extreme_scales():
+    """Keys whose codes are all E4M3 subnormals under a scale of 2^30, and keys whose scale bytes are
+    160..170 (factors beyond the bf16 range of a single product in the kernel's dequantisation), outrank
+    every ordinary key by orders of magnitude: the Top-K holds all of them only if the kernel keeps
+    subnormal codes and large scales exact.  The selection is checked against the oracle in full."""
+    wl = make_workload("mx_extreme", 77, [300, 1000], [1, 1], idx_heads=64, idx_dim=128, idx_fp8=True,
+                       idx_mx=True, top_k=64, attn_heads=16)
+    rng = np.random.default_rng(5)
+    special = []
+    for b in range(wl.batch):
+        L = int(wl.seq_lens[b])
+        for j, pos in enumerate(rng.choice(L, 40, replace=False)):
+            pg, r = int(wl.page_table[b, pos // 64]), int(pos % 64)
+            if j < 20:  # codes 0x01..0x07 with random signs
+                wl.k_cache[pg, r] = (rng.integers(1, 8, 128) | (rng.integers(0, 2, 128) << 7)).astype(np.uint8)
+                wl.k_scale[pg, r] = 127 + 30
+            else:
+                wl.k_scale[pg, r] = rng.integers(160, 171, 4).astype(np.uint8)
+            special.append((b, int(pos)))
+    dw = DeviceWorkload(wl)
+    dw.indexer()
+    assert dw.error_word() == 0
+    topk = dw.topk_host()
+    check_topk(wl, topk)
+    for b, pos in special:
+        assert pos in set(topk[b].tolist()), f"sequence {b}: position {pos} not selected"
