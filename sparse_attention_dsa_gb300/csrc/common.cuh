@@ -79,6 +79,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
 __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
 }
+// The same copy with an L2 cache policy (createpolicy), e.g. evict-first for rows read once per step.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst_smem, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "l"(policy)
+                 : "memory");
+}
 // 16 zero bytes through the same path (no global read: source size 0).
 __device__ __forceinline__ void cp_async_zero16(uint32_t dst_smem, const void* any_valid_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst_smem), "l"(any_valid_src) : "memory");

@@ -352,6 +352,11 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 if (i + 1 < ntiles) load_tile(i + 1);
             }
         } else {
+            // The selected rows are read once per step (by both CTAs of a pair, within a tile period): an
+            // evict-first L2 policy keeps their 75 MB stream from pushing the kernel's code and the step's
+            // other inputs out of L2 (code fetched from HBM made the first tiles several us slower).  The
+            // FP8 rows above keep plain loads: the hinted loads measured slower there.
+            const uint64_t kvpol = l2_policy_evict_first();
             for (int i = 0; i < ntiles; ++i) {
                 const int bsel = i & 1;
                 uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
@@ -369,7 +374,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                         if (is_v_atom(a, dvh) != v_part) continue;
                         const uint32_t dst = row_base + part_slot(a, dvh) * kAtomBytes;
                         if (row >= 0)
-                            cp_async_16(dst, src + a * 64);
+                            cp_async_16_hint(dst, src + a * 64, kvpol);
                         else
                             cp_async_zero16(dst, p.kv_cache);
                     }
