@@ -38,7 +38,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 384;  // threads of the standalone indexer kernel (warps 6-11 join the select)
+constexpr int kThreads = 384;  // threads of the standalone indexer kernel (warps 10-11 only join the select)
 constexpr int kMaxWarps = 16;  // select scratch sized for up to 512 threads
 constexpr int kTileM = 128;  // positions per tile (two pages)
 constexpr int kPage = 64;
@@ -638,7 +638,8 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
 }
 
 // One CTA of the indexer: scoring of this CTA's position range, then the cluster Top-K.  NT threads (the
-// roles use warps 0-5; all NT threads take part in the select).  smem_raw: the dynamic shared memory.
+// scoring roles use warps 0-9: producer, MMA issuer, two epilogue groups or, for MX keys, one epilogue
+// group and four converters; all NT threads take part in the select).  smem_raw: the dynamic shared memory.
 // LAST_TMEM: no later phase of the kernel allocates tensor memory, so the allocation permit is given up
 // after this CTA's allocation.
 template <int HI, int DI, int QB, bool FP8, int NT, bool LAST_TMEM, bool MX = false>
@@ -746,7 +747,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
-            mbar_init(&ctl->tempty[i], 4);  // one arrival per epilogue warp
+            mbar_init(&ctl->tempty[i], 4);  // one arrival per warp of the epilogue group that reads it
         }
         mbar_init(&ctl->qbar, 1);
         for (int i = 0; i < 2; ++i) {
@@ -932,14 +933,19 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 }
             }
             if (lane == 0 && warp == 6) ctl->consumed = consumed;
-        } else if (warp >= 2 && warp < 6) {
+        } else if (warp >= 2 && warp < (MX ? 6 : 10)) {
+            // Two epilogue groups (warps 2-5 take the even tiles, warps 6-9 the odd ones; MX keeps warps
+            // 6-9 for its converters): both groups cover the four TMEM lane quadrants, and an accumulator
+            // buffer is only ever read by one group, so its release count stays four.
+            static_assert(MX || NT >= 320, "the second epilogue group is warps 6-9");
+            const int group = (warp - 2) >> 2;
             const uint32_t quad = (uint32_t)(warp & 3);  // TMEM lanes this warp may access
             const int row = (int)quad * 32 + lane;       // position within the tile
             const uint32_t tmem = ctl->tmem_base + ((quad * 32u) << 16);
             int64_t pq[QB];
 #pragma unroll
             for (int q = 0; q < QB; ++q) pq[q] = (int64_t)L - n_b + j0 + q;
-            for (int i = 0; i < ntiles; ++i) {
+            for (int i = group; i < ntiles; i += (MX ? 1 : 2)) {
                 const int ab = i % Cfg::kAccBufs;
                 const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
                 const int local = i * kTileM + row;
