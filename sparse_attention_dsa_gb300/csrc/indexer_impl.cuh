@@ -964,7 +964,10 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     // keep the FMA chains short, and the weights come four at a time.
 #pragma unroll
                     for (int q = 0; q < QB; ++q) {
-                        float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        // partial sums in pairs (2k, 2k+1), advanced by the packed fp32x2 FMA: one instruction
+                        // per two heads, each lane of it the same rounding as a scalar FMA
+                        float2 part[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                          make_float2(0.f, 0.f)};
 #pragma unroll 1
                         for (int c0 = q * HI; c0 < (q + 1) * HI; c0 += 32) {
                             float v0[16], v1[16];
@@ -978,13 +981,13 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                             for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 wv = w4[j4];
                                 const float* v = j4 < 4 ? v0 + 4 * j4 : v1 + 4 * (j4 - 4);
-                                part[(2 * j4) & 7] = fmaf(wv.x, fmaxf(v[0], 0.f), part[(2 * j4) & 7]);
-                                part[(2 * j4 + 1) & 7] = fmaf(wv.y, fmaxf(v[1], 0.f), part[(2 * j4 + 1) & 7]);
-                                part[(2 * j4) & 7] = fmaf(wv.z, fmaxf(v[2], 0.f), part[(2 * j4) & 7]);
-                                part[(2 * j4 + 1) & 7] = fmaf(wv.w, fmaxf(v[3], 0.f), part[(2 * j4 + 1) & 7]);
+                                float2& pk = part[j4 & 3];
+                                pk = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(fmaxf(v[0], 0.f), fmaxf(v[1], 0.f)), pk);
+                                pk = __ffma2_rn(make_float2(wv.z, wv.w), make_float2(fmaxf(v[2], 0.f), fmaxf(v[3], 0.f)), pk);
                             }
                         }
-                        acc[q] = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                        acc[q] = ((part[0].x + part[0].y) + (part[1].x + part[1].y)) +
+                                 ((part[2].x + part[2].y) + (part[3].x + part[3].y));
                     }
                 } else
 #pragma unroll
