@@ -232,11 +232,26 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """The source without // comments, trailing blanks and empty lines (the kernel sources use no block
+    comments and no // inside string literals), so that a comment edit does not mark a profile stale."""
+    lines = []
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line:
+            lines.append(line)
+    return "\n".join(lines)
+
+
 def source_sha(kernel: str) -> str:
+    """Hash of the code (comments excluded) of the files a kernel is built from."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "sparse_attention_dsa_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparse_attention_dsa_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

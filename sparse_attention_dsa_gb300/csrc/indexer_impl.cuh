@@ -20,9 +20,12 @@
 //   warp 0  : TMA producer.  Each 128-position tile is two 64-token pages of the indexer K cache,
 //             fetched with 3-D tensor-map loads (page id from the page table) into 128B-swizzled smem.
 //   warp 1  : tcgen05 issuer.  D[128 positions, N] = K_tile[128, Di] * Qblk[N, Di]^T with
-//             N = QB*Hi (padded to 16), accumulated in fp32 in tensor memory (two buffers).
-//   warps 2-5: epilogue.  Each thread owns one TMEM lane (= one position), reads its N columns and
-//             reduces sum_h w*max(0, acc) per query (FP8: times the key row scale), then stores the key.
+//             N = QB*Hi (padded to 16), accumulated in fp32 in tensor memory (two or four buffers).
+//   warps 2-5 and 6-9: two epilogue groups (even and odd tiles).  Each thread owns one TMEM lane
+//             (= one position), reads its N columns and reduces sum_h w*max(0, acc) per query (FP8:
+//             times the key row scale), then stores the key.
+//   MXFP8 keys: warps 6-9 instead dequantise each landed tile to bf16 into tensor memory (the MMA's A
+//             operand), and warps 2-5 are the only epilogue group.
 //   other warps: idle during scoring; every warp takes part in the selection.
 #pragma once
 
