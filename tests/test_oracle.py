@@ -464,3 +464,34 @@ def test_mx_scores_equal_bf16_scores_on_the_same_values():
     for t in range(wl.total_q):
         assert np.array_equal(oracle.index_scores(wl, t), scores_mx[t])
     assert np.array_equal(oracle.indexer_topk(wl)[0], top_mx)
+
+
+def test_mx_scores_at_extreme_scales_match_a_direct_evaluation():
+    """Keys made only of subnormal E4M3 codes under a scale of 2^30, and keys with scale bytes 160..170
+    (factors near 2^43), against a float64 evaluation written from the definitions: codes decoded by
+    torch's float8_e4m3fn, scale bytes as 2^(e - 127), then sum_h w * max(0, q . k) per position."""
+    wl = _small(idx_fp8=True, idx_mx=True, idx_heads=3, idx_dim=64, top_k=16, seq_lens=(150, 70), q_lens=(1, 2))
+    rng = np.random.default_rng(9)
+    for b in range(wl.batch):
+        for j, pos in enumerate(rng.choice(int(wl.seq_lens[b]), 12, replace=False)):
+            pg, r = int(wl.page_table[b, pos // wl.page_size]), int(pos % wl.page_size)
+            if j < 6:
+                wl.k_cache[pg, r] = (rng.integers(1, 8, 64) | (rng.integers(0, 2, 64) << 7)).astype(np.uint8)
+                wl.k_scale[pg, r] = 127 + 30
+            else:
+                wl.k_scale[pg, r] = rng.integers(160, 171, 2).astype(np.uint8)
+    e8m0 = lambda e: np.ldexp(1.0, e.astype(np.int64) - 127)
+    qv = _torch_e4m3_value(wl.q_idx.reshape(-1, 64)).reshape(wl.q_idx.shape) * np.repeat(e8m0(wl.q_scale), 32, axis=-1)
+    got = oracle.index_scores_batch(wl, list(range(wl.total_q)))
+    pos_all = wl.query_positions()
+    for t in range(wl.total_q):
+        b = int(wl.query_seq()[t])
+        p = int(pos_all[t])
+        rows = np.arange(p + 1)
+        pages = wl.page_table[b, rows // wl.page_size]
+        codes = wl.k_cache[pages, rows % wl.page_size]
+        kv = _torch_e4m3_value(codes) * np.repeat(e8m0(wl.k_scale[pages, rows % wl.page_size]), 32, axis=-1)
+        dots = kv @ qv[t].T  # [positions, heads]
+        ref = (np.maximum(dots, 0.0) * wl.w[t].astype(np.float64)).sum(axis=1)
+        np.testing.assert_allclose(got[t], ref, rtol=1e-12, atol=0.0)
+        assert np.abs(ref).max() > 1e12  # the large scales are in play
