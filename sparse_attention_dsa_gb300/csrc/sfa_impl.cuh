@@ -23,7 +23,8 @@
 //     with cp.async pieces written straight into the 128B-swizzled operand layout (per-lane 16-byte
 //     copies issue faster here than TMA tile::gather4, which moves only 4 rows per copy).  The loads of
 //     a tile are issued about two tiles ahead of its use, which hides the HBM latency without an L2
-//     prefetch;
+//     prefetch; bf16 rows are copied under an evict-first L2 policy (read once per step, they would
+//     otherwise push the kernel's own code out of L2);
 //   * the MMA issuer runs S(i) = Q K(i)^T over the K part, then O += P(i-1) V(i-1), then the V-part
 //     atoms of S(i).  The V buffer of a tile is busy until its P V has run, so this order gives its
 //     refill a whole tile period; the K buffer is free as soon as the K-part MMAs of S(i) complete;
@@ -32,8 +33,9 @@
 //   * O += P V (M=128, N=256, K=64; A = P from TMEM, B = the V part read as an MN-major operand)
 //     accumulates in TMEM.  The 512 value dims are split between the two CTAs of the pair (each owns 256
 //     columns of O) because a full 128 x 512 fp32 O would fill all of TMEM; both CTAs compute the same S.
-//   * With more than one position split, the partial (O, max, sum) of the splits are merged through
-//     distributed shared memory inside the cluster.
+//   * With more than one position split, the partial (O, max, sum) of the splits are merged through L2:
+//     bulk copies of the rows each split owns into the workspace, one cluster barrier, bulk copies back,
+//     and a combine straight from TMEM.
 #pragma once
 
 #include <cuda_runtime.h>
