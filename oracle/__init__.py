@@ -54,10 +54,11 @@ class _Dims(ctypes.Structure):
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle (gcc -O2 -fopenmp; no fast-math, so IEEE double semantics hold)."""
+    """Compile the oracle (gcc -O3 -fopenmp; no fast-math and no contraction into fused multiply-adds, so
+    every product and sum is the IEEE double operation the C source writes)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        subprocess.check_call(["gcc", "-O3", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -89,6 +90,8 @@ def lib():
             L.oracle_quantize_group.argtypes = [vp, i32, vp, vp]
             L.oracle_append_rows.restype = ctypes.c_int
             L.oracle_append_rows.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 8
+            L.oracle_set_threads.restype = ctypes.c_int
+            L.oracle_set_threads.argtypes = [ctypes.c_int]
             _lib = L
     return _lib
 
@@ -213,3 +216,8 @@ def append(wl, k_new=None, kv_new=None):
 def e8m0_value(e: int) -> float:
     """OCP MX E8M0 scale byte: 2^(e - 127); 0xFF is NaN."""
     return float(lib().oracle_e8m0_value(e))
+
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's parallel loops from now on; returns the previous maximum."""
+    return int(lib().oracle_set_threads(int(n)))

@@ -48,6 +48,7 @@
  *    the precision of the GPU kernel, so both make the same integer decisions.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -71,6 +72,14 @@ typedef struct {
 } oracle_dims;
 
 enum { ORC_OK = 0, ORC_BAD_ARG = -1, ORC_BAD_PAGE = -2, ORC_BAD_POS = -3, ORC_NOMEM = -4 };
+
+/* Threads the oracle's parallel loops use from now on (n >= 1); returns the previous maximum.  Used to
+ * time the oracle on one core. */
+int oracle_set_threads(int n) {
+    int old = omp_get_max_threads();
+    if (n >= 1) omp_set_num_threads(n);
+    return old;
+}
 
 /* bf16 is the upper half of an IEEE binary32 value. */
 double oracle_bf16_value(uint16_t bits) {
@@ -211,36 +220,44 @@ int64_t oracle_index_scores(const oracle_dims* d, const void* q_idx, const float
     int rc = query_locate(d, seq_lens, cu_q_lens, t, &b, &p);
     if (rc) return rc;
     const int32_t H = d->idx_heads, D = d->idx_dim;
-    double* q = (double*)malloc(sizeof(double) * (size_t)H * (size_t)D);
+    /* qT[j][h] = q[t,h,j]: the query stored dimension-major, so that the dot products of all heads advance
+     * together, one dimension at a time.  Every dot product still adds its terms in dimension order
+     * (j = 0, 1, ...), exactly as the definition reads; only independent dot products are interleaved. */
+    double* qT = (double*)malloc(sizeof(double) * (size_t)H * (size_t)D);
     double* k = (double*)malloc(sizeof(double) * (size_t)D);
-    if (!q || !k) {
-        free(q);
+    double* dot = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!qT || !k || !dot) {
+        free(qT);
         free(k);
+        free(dot);
         return ORC_NOMEM;
     }
     for (int32_t h = 0; h < H; ++h)
         for (int32_t j = 0; j < D; ++j)
-            q[h * D + j] = idx_elem(d, q_idx, q_scale, (int64_t)t * H + h, j);
+            qT[j * H + h] = idx_elem(d, q_idx, q_scale, (int64_t)t * H + h, j);
     for (int64_t s = 0; s <= p; ++s) {
         int64_t row;
         rc = page_row(d, page_table, b, s, &row);
         if (rc) {
-            free(q);
+            free(qT);
             free(k);
+            free(dot);
             return rc;
         }
         for (int32_t j = 0; j < D; ++j) k[j] = idx_elem(d, k_cache, k_scale, row, j);
+        for (int32_t h = 0; h < H; ++h) dot[h] = 0.0;
+        for (int32_t j = 0; j < D; ++j)
+            for (int32_t h = 0; h < H; ++h) dot[h] += qT[j * H + h] * k[j];
         double I = 0.0;
         for (int32_t h = 0; h < H; ++h) {
-            double dot = 0.0;
-            for (int32_t j = 0; j < D; ++j) dot += q[h * D + j] * k[j];
-            double relu = dot > 0.0 ? dot : 0.0;
+            double relu = dot[h] > 0.0 ? dot[h] : 0.0;
             I += (double)w[(int64_t)t * H + h] * relu;
         }
         scores[s] = I;
     }
-    free(q);
+    free(qT);
     free(k);
+    free(dot);
     return p + 1;
 }
 
@@ -352,10 +369,15 @@ int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const void* kv_c
         }
         const int32_t* sel = topk + (int64_t)i * K;
         int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(K > 0 ? K : 1));
-        double* z = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
-        if (!rows || !z) {
+        double* z = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)H);
+        /* the selected rows, decoded once (kv[k][c]), and the queries stored dimension-major (qT[c][h]) */
+        double* kv = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)C);
+        double* qT = (double*)malloc(sizeof(double) * (size_t)C * (size_t)H);
+        if (!rows || !z || !kv || !qT) {
             free(rows);
             free(z);
+            free(kv);
+            free(qT);
 #pragma omp atomic write
             err = ORC_NOMEM;
             continue;
@@ -376,20 +398,36 @@ int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const void* kv_c
         if (bad) {
             free(rows);
             free(z);
+            free(kv);
+            free(qT);
 #pragma omp atomic write
             err = bad;
             continue;
         }
+        for (int32_t k = 0; k < K; ++k)
+            if (rows[k] >= 0)
+                for (int32_t c = 0; c < C; ++c) kv[(int64_t)k * C + c] = kv_elem(d, kv_cache, rows[k], c);
+        for (int32_t h = 0; h < H; ++h)
+            for (int32_t c = 0; c < C; ++c) qT[(int64_t)c * H + h] = oracle_bf16_value(q[((int64_t)t * H + h) * C + c]);
+        /* z[k][h] = scale * sum_c q[t,h,c] kv[k,c]: every dot product adds its terms in dimension order; the
+         * heads' dot products advance together */
+        for (int32_t k = 0; k < K; ++k) {
+            if (rows[k] < 0) continue;
+            double* zk = z + (int64_t)k * H;
+            for (int32_t h = 0; h < H; ++h) zk[h] = 0.0;
+            for (int32_t c = 0; c < C; ++c) {
+                const double v = kv[(int64_t)k * C + c];
+                for (int32_t h = 0; h < H; ++h) zk[h] += qT[(int64_t)c * H + h] * v;
+            }
+            for (int32_t h = 0; h < H; ++h) zk[h] = d->softmax_scale * zk[h];
+        }
         for (int32_t h = 0; h < H; ++h) {
-            const uint16_t* qh = q + ((int64_t)t * H + h) * C;
             double zmax = -INFINITY;
             int32_t count = 0;
             for (int32_t k = 0; k < K; ++k) {
                 if (rows[k] < 0) continue;
-                double dot = 0.0;
-                for (int32_t c = 0; c < C; ++c) dot += oracle_bf16_value(qh[c]) * kv_elem(d, kv_cache, rows[k], c);
-                z[k] = d->softmax_scale * dot;
-                if (z[k] > zmax) zmax = z[k];
+                const double zz = z[(int64_t)k * H + h];
+                if (zz > zmax) zmax = zz;
                 ++count;
             }
             double* o = out + ((int64_t)i * H + h) * V;
@@ -403,17 +441,19 @@ int oracle_sparse_attn(const oracle_dims* d, const uint16_t* q, const void* kv_c
             }
             double denom = 0.0;
             for (int32_t k = 0; k < K; ++k)
-                if (rows[k] >= 0) denom += exp(z[k] - zmax);
+                if (rows[k] >= 0) denom += exp(z[(int64_t)k * H + h] - zmax);
             for (int32_t k = 0; k < K; ++k) {
                 if (rows[k] < 0) continue;
-                double a = exp(z[k] - zmax) / denom;
+                double a = exp(z[(int64_t)k * H + h] - zmax) / denom;
                 if (wrow) wrow[k] = a;
-                for (int32_t v = 0; v < V; ++v) o[v] += a * kv_elem(d, kv_cache, rows[k], v);
+                for (int32_t v = 0; v < V; ++v) o[v] += a * kv[(int64_t)k * C + v];
             }
             lse[(int64_t)i * H + h] = zmax + log(denom);
         }
         free(rows);
         free(z);
+        free(kv);
+        free(qT);
     }
     return err;
 }
