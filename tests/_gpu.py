@@ -95,13 +95,20 @@ class DeviceWorkload:
 
 
 def check_topk(wl, gpu_topk, tlist=None):
-    """Top-K parity for the listed tokens (default: all).  Returns the number of excused positions."""
+    """Top-K parity for the listed tokens (default: all).  Returns the number of excused positions.
+
+    The oracle's scores of every visible position are computed only for the tokens whose selection differs
+    from the oracle's as a set (they decide whether the difference lies inside the excusal band)."""
     tlist = list(range(wl.total_q)) if tlist is None else list(tlist)
     ref, kth, nsel = oracle.indexer_topk(wl, tlist)
-    scores = oracle.index_scores_batch(wl, tlist)
+    differ = [i for i, t in enumerate(tlist)
+              if np.setxor1d(gpu_topk[t][gpu_topk[t] >= 0], ref[i][ref[i] >= 0]).shape[0] > 0]
+    scores = dict(zip(differ, oracle.index_scores_batch(wl, [tlist[i] for i in differ]))) if differ else {}
+    pos = wl.query_positions()
     excused = 0
     for i, t in enumerate(tlist):
-        msg = topk_mismatch(gpu_topk[t], ref[i], scores[i], kth[i], nsel[i])
+        sc = scores[i] if i in scores else np.zeros(int(pos[t]) + 1)  # unused when the sets agree
+        msg = topk_mismatch(gpu_topk[t], ref[i], sc, kth[i], nsel[i])
         assert msg is None, f"token {t}: {msg}"
         g = gpu_topk[t][gpu_topk[t] >= 0]
         excused += int(np.setxor1d(g, ref[i][ref[i] >= 0]).shape[0])

@@ -240,19 +240,17 @@ def test_config_decode(n):
     check_attention(wl, topk, out, lse)
 
 
-def test_config_prefill_sampled():
-    """4096 new tokens over 61440 cached ones: every query is computed on the GPU; the oracle checks a
-    sample that includes the first and last tokens and spans every query block."""
+@pytest.mark.slow
+def test_config_prefill():
+    """4096 new tokens over 61440 cached ones (the prefill chunk): every one of the 4096 queries is checked
+    against the oracle, the Top-K set (with the excusal band) and the attention output element by element."""
     wl = config(4)
     dw = DeviceWorkload(wl).fused()
     assert dw.error_word() == 0
     topk = dw.topk_host()
-    sample = sorted({0, 1, 2, 3, 4, 1023, 2047, 2048, 4094, 4095} | set(range(5, 4095, 331)))
-    check_topk(wl, topk, sample)
+    check_topk(wl, topk)
     out, lse = dw.out_host()
-    check_attention(wl, topk, out, lse, sample)
-    # properties every query must satisfy
+    check_attention(wl, topk, out, lse)
     pos = wl.query_positions()
     valid = topk >= 0
     assert np.all(valid.sum(axis=1) == np.minimum(wl.top_k, pos + 1))
-    assert np.all(np.where(valid, topk, -1).max(axis=1) <= pos)
