@@ -52,6 +52,10 @@ def parse_args(argv=None):
                     help="MXFP8 indexer inputs (E4M3 codes, one E8M0 scale per 32 elements)")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="latent-KV cache in the FP8 row layout (one scale per 128 elements of each token)")
+    ap.add_argument("--no-prefill-indexer", action="store_true",
+                    help="skip the prefill-chunk indexer measurement (the tensor-bound half of the path)")
+    ap.add_argument("--clock-window-s", type=float, default=1.0,
+                    help="seconds of back-to-back repeats of the timed steps, sampled for clocks")
     return ap.parse_args(argv)
 
 
@@ -302,6 +306,24 @@ def cpu_baseline(wl, budget_s=20.0):
                       f"attention, float64 C oracle, OpenMP over tokens), {total:.1f} s"}
 
 
+def cpu_single_thread():
+    """The oracle on one core: the 4K-context decode token and one sequence of the 32K-context decode."""
+    import oracle
+    from gen.workloads import config
+
+    old = oracle.set_threads(1)
+    res = {}
+    try:
+        for name, wl in (("decode_b1_ctx4096", config(1)), ("decode_ctx32768_one_sequence", config(2, batch=1))):
+            t0 = time.perf_counter()
+            oracle_step(wl, list(range(wl.total_q)))
+            dt = time.perf_counter() - t0
+            res[name] = {"value": wl.total_q / dt, "unit": UNIT, "seconds": dt}
+    finally:
+        oracle.set_threads(old)
+    return {"cores": 1, "kind": "oracle", **res}
+
+
 def run_reference(args, wl_cfg):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -333,6 +355,67 @@ def run_reference(args, wl_cfg):
 # ------------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------------
+def measure_prefill_indexer(dev, steps: int, warmup: int, gpu_id: str):
+    """The tensor-bound half of the path: the indexer + Top-K of the prefill chunk (4096 new tokens after
+    61440 cached ones, 64 x 128 bf16 heads, K = 2048) through dsa_indexer_topk, each call timed with CUDA
+    events on its stream, inputs resident.  Algorithmic flops: 2 * Hi * Di per (query, visible position)."""
+    import torch
+
+    import sparse_attention_dsa_gb300 as dsa
+    from gen.workloads import config
+
+    wl = config(4, with_sfa=False)
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    d = dsa.DsaDims(batch=wl.batch, total_q=wl.total_q, max_q_len=wl.max_q_len, num_pages=wl.num_pages,
+                    page_size=wl.page_size, max_pages_per_seq=wl.max_pages_per_seq, idx_heads=wl.idx_heads,
+                    idx_dim=wl.idx_dim, idx_dtype=dsa.DSA_BF16, top_k=wl.top_k, attn_heads=128, kv_dim=576,
+                    v_dim=512, softmax_scale=wl.softmax_scale, kv_dtype=dsa.DSA_BF16)
+    q_idx, w, k_cache = up(wl.q_idx), up(wl.w), up(wl.k_cache)
+    pt, sl, cu = up(wl.page_table), up(wl.seq_lens), up(wl.cu_q_lens)
+    topk = torch.empty((wl.total_q, wl.top_k), dtype=torch.int32, device=dev)
+    ws = torch.zeros((dsa.workspace_size(d) + 3) // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        dsa.indexer_topk(d, q_idx, None, w, k_cache, None, pt, sl, cu, topk, ws, stream)
+
+    for _ in range(max(warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id).start()
+    n = max(steps, 5)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    t0 = time.time()
+    for i in range(n):
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    # clocks: repeats of the same calls for about half a second around the timed ones
+    while time.time() - t0 < 0.5:
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    if dsa.get_device_error(ws, stream) != 0:
+        raise RuntimeError("device error word set in the prefill indexer measurement")
+    ms = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
+    flops = indexer_flops(wl)
+    tflops = flops / (ms * 1e-3) / 1e12
+    _, tc_peak, tc_kind = measured_peaks()
+    return {"workload": "prefill_q4096_ctx65536_hi64x128_bf16_k2048", "ms": ms, "achieved": tflops, "unit": "TFLOP/s",
+            "peak": tc_peak, "frac": tflops / tc_peak, "algorithmic_flops": flops, "calls": n,
+            "peak_source": f"{tc_kind} bf16_tflops (MEASURED_PEAKS.json)" if tc_kind == "measured" else
+            "fallback 1900 TF/s",
+            "timing": "median of per-call CUDA event pairs on the launching stream, inputs resident (17 MB of keys: "
+                      "L2-resident between calls, as in a prefill pass over the chunk's queries)",
+            "clocks": sampler.summary(t0, t1)}
+
 def run_ours(args):
     import torch
 
@@ -404,6 +487,18 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_host1 = time.time()
     barrier(dist)
+    # clock window: the timed steps are repeated back to back, in blocks of K timed the same way, until the
+    # window is long enough for the sampler (every 20 ms) to see the GPU under exactly this load
+    block_ms = []
+    while time.time() - t_host0 < args.clock_window_s:
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for i in range(K):
+            step()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        block_ms.append(b0.elapsed_time(b1) / K)
+    t_window1 = time.time()
     # launch durations for the roofline: the same steps with an event pair around each one
     launches_per_step = dsa.fused_decode_launches(d)
     ev_step = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
@@ -420,8 +515,19 @@ def run_ours(args):
         dsa.sparse_attn(d, q, kv, pt, sl, cu, topk, out, lse, ws, stream)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
+    # cold L2: every step preceded by a 512 MB write (4x the 129 MB L2), timed with its own event pair
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    ev_cold = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev_cold[i][0].record(stream)
+        step()
+        ev_cold[i][1].record(stream)
+    torch.cuda.synchronize()
+    del flush
     sampler.stop()
     total_ms = start.elapsed_time(end)
+    cold_ms = sum(e[0].elapsed_time(e[1]) for e in ev_cold) / K
     step_ms = sum(e[0].elapsed_time(e[1]) for e in ev_step) / K
     idx_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     sfa_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
@@ -541,18 +647,28 @@ def run_ours(args):
         "config": {"workload": workload_name(args), "batch_per_gpu": wl.batch, "seq_len": int(wl.seq_lens.max()),
                    "query_tokens_per_gpu": T, "top_k": wl.top_k, "idx_heads": wl.idx_heads, "idx_dim": wl.idx_dim,
                    "attn_heads": wl.attn_heads, "kv_dim": wl.kv_dim, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (indexer K cache and latent-KV cache exceed 129 MB); no flush"},
+                   "l2": "inputs larger than L2 (indexer K cache and latent-KV cache exceed 129 MB); no flush "
+                         "in the timed steps; cold_l2 repeats them with a 512 MB flush before each"},
         "kernel_ms": {"step_launch" if launches_per_step == 1 else "step": step_ms,
                       "indexer_separate": idx_ms, "sparse_attn_separate": sfa_ms},
         "launches_per_step": launches_per_step,
         "step_bytes": step_bytes, "step_hbm_frac": step_bytes / (t_max_s / K) / 1e9 / hbm_peak,
         "roofline": roofline, "gpu_launches": launches_per_step * K,
-        "clocks": sampler.summary(t_host0, t_host1),
+        "clocks": dict(sampler.summary(t_host0, t_window1),
+                       window=f"the {K} timed steps and {len(block_ms)} back-to-back repeats of them "
+                              f"({t_window1 - t_host0:.2f} s)",
+                       repeat_ms_per_step_median=float(np.median(block_ms)) if block_ms else None),
+        "cold_l2": {"ms_per_step": cold_ms, "value": T * world / (cold_ms * 1e-3), "unit": UNIT,
+                    "hbm_frac": step_bytes / (cold_ms * 1e-3) / 1e9 / hbm_peak,
+                    "how": "each step preceded by a 512 MB device write (L2 is 129 MB), per-step CUDA event pairs"},
     }
     if e2e is not None:
         result["e2e"] = e2e
+    if not args.no_prefill_indexer and args.config != 4:
+        result["prefill_indexer"] = measure_prefill_indexer(dev, K, args.warmup, gpu_id)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
+        result["cpu_baseline"]["single_thread"] = cpu_single_thread()
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
