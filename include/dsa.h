@@ -14,7 +14,8 @@
  *       sections 2.1 (deep operator fusion) and 3.1 (FP8 indexer inputs).
  *  [A4] "Day0 Inference Support and Performance Optimization for New LLM Architectures", sections 3.1
  *       (integrated indexer fusion), 3.2 (sparse attention kernel), 3.3 (input preparation ahead of the
- *       indexer) and 4 (hierarchical quantization: "Token-Head-Tile" FP8 KV cache, tiles of 128).
+ *       indexer), 4 (hierarchical quantization: "Token-Head-Tile" FP8 KV cache, tiles of 128) and 5
+ *       (context parallelism: 5.1 decode by context shards, 5.2 the Zigzag layout of prefill).
  *
  * Conventions shared by every entry point
  *  - Ownership: the caller owns every buffer.  All array arguments are DEVICE pointers (memory of the
@@ -46,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 
 typedef enum {
     DSA_OK = 0,
@@ -82,7 +83,8 @@ typedef enum {
 #define DSA_DEVERR_PAGE 0x1    /* a page-table entry outside [0, num_pages) was needed */
 #define DSA_DEVERR_SEQ 0x2     /* n_b > L_b, or L_b > max_pages_per_seq * page_size */
 #define DSA_DEVERR_INDEX 0x4   /* a Top-K entry outside [-1, p] reached the attention kernel */
-#define DSA_DEVERR_TIMEOUT 0x8 /* a pipeline wait exceeded its limit (about one second) */
+#define DSA_DEVERR_TIMEOUT 0x8 /* a pipeline wait exceeded its limit (one second unless
+                                  dsa_set_wait_limit_ns() says otherwise) */
 
 typedef struct {
     int32_t batch;             /* B >= 1 sequences */
@@ -129,8 +131,8 @@ size_t dsa_workspace_size(const dsa_dims_t* dims);
  * Lightning indexer + Top-K ([A2] step 1; [A3] 2.1; [A4] 3.1): for every query token t,
  *     I[t,s] = sum_h w[t,h] * max(0, q_idx[t,h,:] . k[s,:])      for s = 0..p_t,
  * and keep the K positions with the largest I (ties: the lower position wins).  The scores stay on
- * chip; only the selected positions are written.  With FP8 inputs, q_idx[t,h,:] and k[s,:] are the
- * codes times their row scales.
+ * chip; only the selected positions (and, on request, their scores) are written.  With FP8 inputs,
+ * q_idx[t,h,:] and k[s,:] are the codes times their row scales.
  *   q_idx        [T, Hi, Di]  bf16, or E4M3 codes (uint8) when dims->idx_dtype is DSA_FP8_E4M3 or
  *                DSA_MXFP8_E4M3
  *   q_scale      [T, Hi] fp32 row scales of q_idx (DSA_FP8_E4M3), [T, Hi, Di/32] E8M0 bytes
@@ -142,6 +144,9 @@ size_t dsa_workspace_size(const dsa_dims_t* dims);
  *   page_table   [B, max_pages_per_seq] int32;  seq_lens [B] int32;  cu_q_lens [B+1] int32
  *   topk_idx     [T, K] int32 output: the selected positions of each query in ascending order; when
  *                fewer than K positions are visible all of them are kept and the rest is -1.
+ *   topk_score   [T, K] fp32 output or NULL: I[t, topk_idx[t,k]] as the kernel computed it (fp32
+ *                accumulation; -0 is written as +0), -inf where topk_idx is -1.  These are the keys
+ *                dsa_topk_merge orders by.
  *   workspace    dsa_workspace_size(dims) bytes (see above)
  * Supported: (Hi, Di) = (4, 64) or (64, 128) in bf16, (64, 128) in FP8 and MXFP8; K <= 4096 (MXFP8 runs
  * one query token per thread-block cluster, any number per sequence).
@@ -149,7 +154,39 @@ size_t dsa_workspace_size(const dsa_dims_t* dims);
 dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
                               const void* k_cache, const void* k_scale, const int32_t* page_table,
                               const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx,
-                              void* workspace, void* stream);
+                              float* topk_score, void* workspace, void* stream);
+
+/*
+ * dsa_indexer_topk restricted to the positions of one context shard ([A4] 5.1: under context
+ * parallelism each device scores the positions it holds and keeps a local Top-K of (score, position)):
+ * only positions s with pos_begin <= s < pos_end (and s <= p_t) are candidates; the result holds the K
+ * best of them (all of them, -1 padded, if there are fewer), in ascending order, with their scores.
+ * Positions are the sequence's logical positions; page_table entries of pages outside the range are
+ * never read (a shard's table may hold anything there).  pos_begin must be a multiple of 64 (page
+ * aligned); pos_end > pos_begin (INT32_MAX: to the end).  Other arguments and limits as for
+ * dsa_indexer_topk.  Selecting each shard's Top-K and merging them with dsa_topk_merge gives exactly the
+ * selection of dsa_indexer_topk over the whole context (the scores of a position do not depend on the
+ * range it is scored in).
+ */
+dsa_status_t dsa_indexer_topk_shard(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
+                                    const void* k_cache, const void* k_scale, const int32_t* page_table,
+                                    const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t pos_begin,
+                                    int32_t pos_end, int32_t* topk_idx, float* topk_score, void* workspace,
+                                    void* stream);
+
+/*
+ * Merge of context-shard selections ([A4] 5.1: the shards' local Top-K lists are gathered and merged
+ * into the global Top-K with the same key).  For every query token t, from the candidates
+ * (topk_idx[s,t,k], topk_score[s,t,k]) of all shards s (entries with topk_idx < 0 are empty), keep the K
+ * with the largest score, ties to the lower position; write them in candidate order (shard 0 first),
+ * which is ascending when shard s holds positions below those of shard s+1 and each list is ascending
+ * (as dsa_indexer_topk_shard writes them), then -1 / -inf padding.
+ *   topk_idx    [shards, T, K] int32;  topk_score [shards, T, K] fp32 (from dsa_indexer_topk_shard)
+ *   out_idx     [T, K] int32 output;   out_score  [T, K] fp32 output or NULL
+ * Positions must be distinct across shards.  No workspace.  Supported: shards * K <= 16384.
+ */
+dsa_status_t dsa_topk_merge(int32_t shards, int32_t total_q, int32_t top_k, const int32_t* topk_idx,
+                            const float* topk_score, int32_t* out_idx, float* out_score, void* stream);
 
 /*
  * Sparse flash attention over the selected rows ([A2] step 2; [A4] 3.2; [A1] 3.2): for every query
@@ -169,6 +206,30 @@ dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const v
 dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* kv_cache, const int32_t* page_table,
                              const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out,
                              float* lse, void* workspace, void* stream);
+
+/*
+ * dsa_sparse_attn over the selected rows one context shard holds ([A4] 5.1: each device attends to the
+ * selected rows in its own cache, giving a partial (out, lse)): entries of topk_idx outside
+ * [pos_begin, pos_end) are skipped like -1 (they are not an error).  out and lse are the attention over
+ * the shard's rows alone (out = 0 and lse = -inf when it holds none); dsa_attn_combine joins the
+ * shards' partials.  Other arguments and limits as for dsa_sparse_attn.
+ */
+dsa_status_t dsa_sparse_attn_shard(const dsa_dims_t* dims, const void* q, const void* kv_cache,
+                                   const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                   const int32_t* topk_idx, int32_t pos_begin, int32_t pos_end, void* out, float* lse,
+                                   void* workspace, void* stream);
+
+/*
+ * Combine of partial attention results ([A4] 5.1: the shards' partial outputs are merged with their
+ * log-sum-exp values): for every token t and head h,
+ *     LSE = log sum_s exp(lse_parts[s,t,h]),   out[t,h,:] = sum_s exp(lse_parts[s,t,h] - LSE) * out_parts[s,t,h,:]
+ * (shards with lse = -inf have weight 0; with none left, out = 0 and lse = -inf).
+ *   out_parts [shards, T, heads, v_dim] bf16;  lse_parts [shards, T, heads] fp32
+ *   out       [T, heads, v_dim] bf16 output;   lse [T, heads] fp32 output or NULL
+ * Arithmetic in fp32.  No workspace.  v_dim must be even.
+ */
+dsa_status_t dsa_attn_combine(int32_t shards, int32_t total_q, int32_t heads, int32_t v_dim, const void* out_parts,
+                              const float* lse_parts, void* out, float* lse, void* stream);
 
 /*
  * The whole decode/prefill step: the work of dsa_indexer_topk followed by that of dsa_sparse_attn on
@@ -202,18 +263,21 @@ int32_t dsa_fused_decode_launches(const dsa_dims_t* dims);
  *   - the scratch (the device error word: the indexer uses only the first 256 bytes of a workspace)
  *     lives in a static device array of 4096 bytes inside the library; every GPU that loads the
  *     library holds it until the process exits;
- *   - device_error (optional DEVICE pointer to one int32, may be NULL) receives this call's device
- *     error word (see dsa_get_device_error) on `stream` after the kernel.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Each call clears the error word
- * on `stream` before launching.  All calls share the one array, so calls that may overlap on the
- * GPU (different streams, or different host threads) race on it.  Nothing is allocated: no cudaMalloc,
- * cudaFree or allocating library routine is called.
+ *   - device_error (optional DEVICE pointer to one int32, 4-byte aligned) receives this call's device
+ *     error word (see dsa_get_device_error) on `stream` after the kernel.  With NULL the word is
+ *     discarded: device-side problems (bad pages, lengths, a wait that gave up) are then not reported.
+ * Every call looks up the array's device address in the current device's context
+ * (cudaGetSymbolAddress, with that device current; this allocates nothing).  Every argument is checked
+ * first: a call that returns an error has put nothing on `stream` and left *device_error unchanged.
+ * Otherwise the call clears the error word on `stream`, launches, and copies the word out.  All calls
+ * share the one array, so calls that may overlap on the GPU (different streams, or different host
+ * threads) race on it.  Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine is
+ * called.
  */
 dsa_status_t dsa_indexer_topk_static(const dsa_dims_t* dims, const void* q_idx, const void* q_scale,
                                      const float* w, const void* k_cache, const void* k_scale,
                                      const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
-                                     int32_t* topk_idx, int32_t* device_error, void* stream);
+                                     int32_t* topk_idx, float* topk_score, int32_t* device_error, void* stream);
 
 /*
  * Synchronises `stream`, then reads the device error word of `workspace` into *code (host pointer).
@@ -244,6 +308,16 @@ dsa_status_t dsa_append_rows(const dsa_dims_t* dims, const void* k_new, const vo
 
 /* Zeroes the device error word (asynchronously on `stream`). */
 dsa_status_t dsa_clear_device_error(void* workspace, void* stream);
+
+/*
+ * Failure detection: sets the limit, in nanoseconds, after which a pipeline wait inside the kernels gives
+ * up (sets DSA_DEVERR_TIMEOUT, abandons its work, and the kernel still drains its copies in flight and
+ * frees its tensor memory under the default limit before it returns).  Applies to launches made after
+ * the call, from any host thread; 0 restores the default of one second.  Returns the previous limit.  A
+ * short limit makes correct launches report DSA_DEVERR_TIMEOUT (with unspecified outputs): it exists to
+ * test that path.  The articles have no counterpart to this call.
+ */
+uint64_t dsa_set_wait_limit_ns(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -26,14 +26,19 @@ from ._lib import (  # noqa: F401
     DsaError,
     abi_version,
     append_rows,
+    attn_combine,
     clear_device_error,
     fused_decode,
     fused_decode_launches,
     get_device_error,
     indexer_topk,
+    indexer_topk_shard,
     indexer_topk_static,
     lib,
+    set_wait_limit_ns,
     sparse_attn,
+    sparse_attn_shard,
     status_string,
+    topk_merge,
     workspace_size,
 )

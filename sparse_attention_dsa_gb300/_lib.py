@@ -32,6 +32,11 @@ EXPORTED = (
     "dsa_clear_device_error",
     "dsa_indexer_topk_static",
     "dsa_append_rows",
+    "dsa_indexer_topk_shard",
+    "dsa_sparse_attn_shard",
+    "dsa_topk_merge",
+    "dsa_attn_combine",
+    "dsa_set_wait_limit_ns",
 )
 
 
@@ -89,7 +94,19 @@ def lib() -> ctypes.CDLL:
             L.dsa_workspace_size.restype = ctypes.c_size_t
             L.dsa_workspace_size.argtypes = [ctypes.POINTER(DsaDims)]
             L.dsa_indexer_topk.restype = st
-            L.dsa_indexer_topk.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 11
+            L.dsa_indexer_topk.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 12
+            L.dsa_indexer_topk_shard.restype = st
+            L.dsa_indexer_topk_shard.argtypes = ([ctypes.POINTER(DsaDims)] + [vp] * 8 + [ctypes.c_int32] * 2 +
+                                                 [vp] * 4)
+            L.dsa_sparse_attn_shard.restype = st
+            L.dsa_sparse_attn_shard.argtypes = ([ctypes.POINTER(DsaDims)] + [vp] * 6 + [ctypes.c_int32] * 2 +
+                                                [vp] * 4)
+            L.dsa_topk_merge.restype = st
+            L.dsa_topk_merge.argtypes = [ctypes.c_int32] * 3 + [vp] * 5
+            L.dsa_attn_combine.restype = st
+            L.dsa_attn_combine.argtypes = [ctypes.c_int32] * 4 + [vp] * 5
+            L.dsa_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.dsa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.dsa_sparse_attn.restype = st
             L.dsa_sparse_attn.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 10
             L.dsa_fused_decode.restype = st
@@ -101,7 +118,7 @@ def lib() -> ctypes.CDLL:
             L.dsa_clear_device_error.restype = st
             L.dsa_clear_device_error.argtypes = [vp, vp]
             L.dsa_indexer_topk_static.restype = st
-            L.dsa_indexer_topk_static.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 11
+            L.dsa_indexer_topk_static.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 12
             L.dsa_append_rows.restype = st
             L.dsa_append_rows.argtypes = [ctypes.POINTER(DsaDims)] + [vp] * 10
             _lib = L
@@ -145,10 +162,45 @@ def workspace_size(dims: DsaDims) -> int:
 
 
 def indexer_topk(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx, workspace,
-                 stream=None):
+                 stream=None, topk_score=None):
     _check(lib().dsa_indexer_topk(ctypes.byref(dims), _ptr(q_idx), _ptr(q_scale), _ptr(w), _ptr(k_cache),
                                   _ptr(k_scale), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q_lens), _ptr(topk_idx),
-                                  _ptr(workspace), _stream(stream)))
+                                  _ptr(topk_score), _ptr(workspace), _stream(stream)))
+
+
+def indexer_topk_shard(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, pos_begin, pos_end,
+                       topk_idx, topk_score, workspace, stream=None):
+    """dsa_indexer_topk_shard: the Top-K of the positions in [pos_begin, pos_end) only, with their scores."""
+    _check(lib().dsa_indexer_topk_shard(ctypes.byref(dims), _ptr(q_idx), _ptr(q_scale), _ptr(w), _ptr(k_cache),
+                                        _ptr(k_scale), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q_lens),
+                                        int(pos_begin), int(pos_end), _ptr(topk_idx), _ptr(topk_score),
+                                        _ptr(workspace), _stream(stream)))
+
+
+def sparse_attn_shard(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, pos_begin, pos_end, out, lse,
+                      workspace, stream=None):
+    """dsa_sparse_attn_shard: attention over the selected rows in [pos_begin, pos_end) (a partial out, lse)."""
+    _check(lib().dsa_sparse_attn_shard(ctypes.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(page_table),
+                                       _ptr(seq_lens), _ptr(cu_q_lens), _ptr(topk_idx), int(pos_begin), int(pos_end),
+                                       _ptr(out), _ptr(lse), _ptr(workspace), _stream(stream)))
+
+
+def topk_merge(shards, total_q, top_k, topk_idx, topk_score, out_idx, out_score=None, stream=None):
+    """dsa_topk_merge: the global Top-K of the shards' (position, score) lists, [shards, T, K] each."""
+    _check(lib().dsa_topk_merge(int(shards), int(total_q), int(top_k), _ptr(topk_idx), _ptr(topk_score),
+                                _ptr(out_idx), _ptr(out_score), _stream(stream)))
+
+
+def attn_combine(shards, total_q, heads, v_dim, out_parts, lse_parts, out, lse=None, stream=None):
+    """dsa_attn_combine: the shards' partial attention outputs joined by their log-sum-exp weights."""
+    _check(lib().dsa_attn_combine(int(shards), int(total_q), int(heads), int(v_dim), _ptr(out_parts),
+                                  _ptr(lse_parts), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    """dsa_set_wait_limit_ns: limit of the kernels' pipeline waits for later launches (0 = one second).
+    Returns the previous limit."""
+    return int(lib().dsa_set_wait_limit_ns(int(limit_ns)))
 
 
 def sparse_attn(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream=None):
@@ -174,11 +226,11 @@ def fused_decode_launches(dims) -> int:
 
 
 def indexer_topk_static(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens, topk_idx,
-                        device_error=None, stream=None):
+                        device_error=None, stream=None, topk_score=None):
     """dsa_indexer_topk_static: no workspace; the library's static device scratch is used instead."""
     _check(lib().dsa_indexer_topk_static(ctypes.byref(dims), _ptr(q_idx), _ptr(q_scale), _ptr(w), _ptr(k_cache),
                                          _ptr(k_scale), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q_lens),
-                                         _ptr(topk_idx), _ptr(device_error), _stream(stream)))
+                                         _ptr(topk_idx), _ptr(topk_score), _ptr(device_error), _stream(stream)))
 
 
 def get_device_error(workspace, stream=None) -> int:

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libdsa_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["api.cu", "indexer.cu", "sfa.cu", "decode.cu", "noalloc.cu", "append.cu"]
+SOURCES = ["api.cu", "indexer.cu", "sfa.cu", "decode.cu", "noalloc.cu", "append.cu", "cp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -8,6 +8,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -17,6 +19,7 @@
 namespace {
 
 thread_local std::string g_last_error;
+std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};  // limit of the kernels' pipeline waits
 
 dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
     char buf[512];
@@ -117,7 +120,13 @@ dsa_status_t check_common(const dsa_dims_t* d) {
 
 constexpr int kMaxClusterSize = 16;
 
-dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::IndexerLaunch* L) {
+// Candidate positions of an indexer call: [pos_begin, pos_end) (the whole context by default).
+struct PosRange {
+    int32_t begin = 0;
+    int32_t end = INT32_MAX;
+};
+
+dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::IndexerLaunch* L, PosRange r = PosRange()) {
     if (d->idx_heads < 1 || d->idx_dim < 1)
         return fail(DSA_ERR_INVALID_ARG, "idx_heads and idx_dim must be >= 1 (got %d, %d)", d->idx_heads, d->idx_dim);
     if (d->idx_dtype != DSA_BF16 && d->idx_dtype != DSA_FP8_E4M3 && d->idx_dtype != DSA_MXFP8_E4M3)
@@ -125,7 +134,8 @@ dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::Index
     const bool mx = d->idx_dtype == DSA_MXFP8_E4M3;
     const bool fp8 = d->idx_dtype == DSA_FP8_E4M3 || mx;  // one-byte codes
     const int quant = mx ? 2 : fp8 ? 1 : 0;
-    const int64_t max_ctx = (int64_t)d->max_pages_per_seq * 64;
+    // the positions one work item scores: the candidate range within the longest context
+    const int64_t max_ctx = std::max<int64_t>(0, std::min<int64_t>((int64_t)d->max_pages_per_seq * 64, r.end) - r.begin);
     int qb_max;
     if (mx) {
         if (d->idx_heads != 64 || d->idx_dim != 128)
@@ -187,7 +197,10 @@ dsa_status_t plan_indexer(const dsa_dims_t* d, const DeviceInfo& dev, dsa::Index
     p.top_k = d->top_k;
     p.qb = qb;
     p.blocks_per_seq = blocks_per_seq;
-    p.chunk = (int)chunk_for(C);
+    p.chunk = (int)chunk_for(C) > 0 ? (int)chunk_for(C) : 128;
+    p.pos_begin = r.begin;
+    p.pos_end = r.end;
+    p.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     return DSA_OK;
 }
 
@@ -225,16 +238,19 @@ dsa_status_t encode_indexer_maps(const dsa_dims_t* d, const void* q_idx, const v
 // Everything of an indexer call but the launch.  *launch is false when there is nothing to launch.
 dsa_status_t prepare_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_scale, const float* w,
                              const void* k_cache, const float* k_scale, const int32_t* page_table,
-                             const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace,
-                             dsa::IndexerLaunch* Lout, bool* launch) {
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, float* topk_score,
+                             void* workspace, dsa::IndexerLaunch* Lout, bool* launch, PosRange range = PosRange()) {
     *launch = false;
     dsa_status_t st = check_common(d);
     if (st) return st;
+    if (range.begin < 0 || range.begin % 64 != 0 || range.end <= range.begin)
+        return fail(DSA_ERR_INVALID_ARG, "position range [%d, %d) must be non-empty with a start that is a multiple of 64",
+                    range.begin, range.end);
     const bool fp8 = d->idx_dtype == DSA_FP8_E4M3 || d->idx_dtype == DSA_MXFP8_E4M3;
     if ((st = check_ptr(q_idx, "q_idx")) || (st = check_ptr(w, "w")) || (st = check_ptr(k_cache, "k_cache")) ||
         (st = check_ptr(page_table, "page_table")) || (st = check_ptr(seq_lens, "seq_lens")) ||
         (st = check_ptr(cu_q_lens, "cu_q_lens")) || (st = check_ptr(topk_idx, "topk_idx")) ||
-        (st = check_ptr(workspace, "workspace")))
+        (st = check_ptr(topk_score, "topk_score", false)) || (st = check_ptr(workspace, "workspace")))
         return st;
     if (fp8 && ((st = check_ptr(q_scale, "q_scale")) || (st = check_ptr(k_scale, "k_scale")))) return st;
     // argument checks that need no device come before the device query
@@ -247,7 +263,7 @@ dsa_status_t prepare_indexer(const dsa_dims_t* d, const void* q_idx, const float
     if ((st = device_info(&dev))) return st;
     dsa::IndexerLaunch& L = *Lout;
     memset(&L, 0, sizeof L);
-    if ((st = plan_indexer(d, dev, &L))) return st;
+    if ((st = plan_indexer(d, dev, &L, range))) return st;
     if (d->total_q == 0) return DSA_OK;
     const int n_cols = dsa::indexer_variant_n(d->idx_heads, d->idx_dim, L.mx ? 2 : fp8 ? 1 : 0, L.params.qb);
     if ((st = encode_indexer_maps(d, q_idx, k_cache, n_cols, &L))) return st;
@@ -260,6 +276,7 @@ dsa_status_t prepare_indexer(const dsa_dims_t* d, const void* q_idx, const float
     p.seq_lens = seq_lens;
     p.cu_q_lens = cu_q_lens;
     p.topk = topk_idx;
+    p.topk_score = topk_score;
     p.err = static_cast<int32_t*>(workspace);
     *launch = true;
     return DSA_OK;
@@ -275,11 +292,12 @@ dsa_status_t launch_indexer_checked(const dsa::IndexerLaunch& L, void* stream) {
 
 dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_scale, const float* w,
                          const void* k_cache, const float* k_scale, const int32_t* page_table, const int32_t* seq_lens,
-                         const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace, void* stream) {
+                         const int32_t* cu_q_lens, int32_t* topk_idx, float* topk_score, void* workspace, void* stream,
+                         PosRange range = PosRange()) {
     dsa::IndexerLaunch L;
     bool launch = false;
     dsa_status_t st = prepare_indexer(d, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens,
-                                      topk_idx, workspace, &L, &launch);
+                                      topk_idx, topk_score, workspace, &L, &launch, range);
     if (st || !launch) return st;
     return launch_indexer_checked(L, stream);
 }
@@ -287,7 +305,7 @@ dsa_status_t run_indexer(const dsa_dims_t* d, const void* q_idx, const float* q_
 // Everything of an attention call but the launch.  *launch is false when there is nothing to launch.
 dsa_status_t prepare_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out,
-                         float* lse, void* workspace, dsa::SfaLaunch* Lout, bool* launch) {
+                         float* lse, void* workspace, dsa::SfaLaunch* Lout, bool* launch, PosRange range = PosRange()) {
     *launch = false;
     dsa_status_t st = check_common(d);
     if (st) return st;
@@ -336,6 +354,9 @@ dsa_status_t prepare_sfa(const dsa_dims_t* d, const void* q, const void* kv_cach
     p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
     p.merge = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kErrorWordArea);
     p.kv_fp8 = d->kv_dtype == DSA_FP8_E4M3 ? 1 : 0;
+    p.pos_begin = range.begin;
+    p.pos_end = range.end;
+    p.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     L.smem_limit = dev.smem_optin;
     L.num_sms = dev.num_sms;
     {
@@ -365,11 +386,11 @@ dsa_status_t launch_sfa_checked(dsa::SfaLaunch L, void* stream, bool after_index
 
 dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, const int32_t* page_table,
                      const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* topk_idx, void* out, float* lse,
-                     void* workspace, void* stream) {
+                     void* workspace, void* stream, PosRange range = PosRange()) {
     dsa::SfaLaunch L;
     bool launch = false;
-    dsa_status_t st =
-        prepare_sfa(d, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, &L, &launch);
+    dsa_status_t st = prepare_sfa(d, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, &L,
+                                  &launch, range);
     if (st || !launch) return st;
     return launch_sfa_checked(L, stream, false);
 }
@@ -377,6 +398,19 @@ dsa_status_t run_sfa(const dsa_dims_t* d, const void* q, const void* kv_cache, c
 }  // namespace
 
 void dsa::set_last_error(const char* message) { g_last_error = message ? message : ""; }
+
+uint64_t dsa::wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+dsa_status_t dsa::prepare_indexer_call(const dsa_dims_t* d, const void* q_idx, const void* q_scale, const float* w,
+                                       const void* k_cache, const void* k_scale, const int32_t* page_table,
+                                       const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx,
+                                       float* topk_score, void* workspace, IndexerLaunch* L, bool* launch) {
+    g_last_error.clear();
+    return prepare_indexer(d, q_idx, static_cast<const float*>(q_scale), w, k_cache, static_cast<const float*>(k_scale),
+                           page_table, seq_lens, cu_q_lens, topk_idx, topk_score, workspace, L, launch);
+}
+
+dsa_status_t dsa::launch_indexer_call(const IndexerLaunch& L, void* stream) { return launch_indexer_checked(L, stream); }
 
 extern "C" {
 
@@ -405,12 +439,25 @@ size_t dsa_workspace_size(const dsa_dims_t* dims) {
 
 dsa_status_t dsa_indexer_topk(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
                               const void* k_cache, const void* k_scale, const int32_t* page_table,
-                              const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, void* workspace,
-                              void* stream) {
+                              const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx, float* topk_score,
+                              void* workspace, void* stream) {
     g_last_error.clear();
     // the scale arrays are fp32 (DSA_FP8_E4M3) or E8M0 bytes (DSA_MXFP8_E4M3); the kernels read them by type
     return run_indexer(dims, q_idx, static_cast<const float*>(q_scale), w, k_cache, static_cast<const float*>(k_scale),
-                       page_table, seq_lens, cu_q_lens, topk_idx, workspace, stream);
+                       page_table, seq_lens, cu_q_lens, topk_idx, topk_score, workspace, stream);
+}
+
+dsa_status_t dsa_indexer_topk_shard(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
+                                    const void* k_cache, const void* k_scale, const int32_t* page_table,
+                                    const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t pos_begin,
+                                    int32_t pos_end, int32_t* topk_idx, float* topk_score, void* workspace,
+                                    void* stream) {
+    g_last_error.clear();
+    PosRange r;
+    r.begin = pos_begin;
+    r.end = pos_end;
+    return run_indexer(dims, q_idx, static_cast<const float*>(q_scale), w, k_cache, static_cast<const float*>(k_scale),
+                       page_table, seq_lens, cu_q_lens, topk_idx, topk_score, workspace, stream, r);
 }
 
 dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* kv_cache, const int32_t* page_table,
@@ -418,6 +465,81 @@ dsa_status_t dsa_sparse_attn(const dsa_dims_t* dims, const void* q, const void* 
                              float* lse, void* workspace, void* stream) {
     g_last_error.clear();
     return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream);
+}
+
+dsa_status_t dsa_sparse_attn_shard(const dsa_dims_t* dims, const void* q, const void* kv_cache,
+                                   const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                   const int32_t* topk_idx, int32_t pos_begin, int32_t pos_end, void* out, float* lse,
+                                   void* workspace, void* stream) {
+    g_last_error.clear();
+    if (pos_begin < 0 || pos_end <= pos_begin)
+        return fail(DSA_ERR_INVALID_ARG, "position range [%d, %d) must be non-empty and non-negative", pos_begin, pos_end);
+    PosRange r;
+    r.begin = pos_begin;
+    r.end = pos_end;
+    return run_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, stream, r);
+}
+
+dsa_status_t dsa_topk_merge(int32_t shards, int32_t total_q, int32_t top_k, const int32_t* topk_idx,
+                            const float* topk_score, int32_t* out_idx, float* out_score, void* stream) {
+    g_last_error.clear();
+    if (shards < 1 || total_q < 0 || top_k < 1)
+        return fail(DSA_ERR_INVALID_ARG, "need shards >= 1, total_q >= 0, top_k >= 1 (got %d, %d, %d)", shards, total_q,
+                    top_k);
+    dsa_status_t st;
+    if ((st = check_ptr(topk_idx, "topk_idx")) || (st = check_ptr(topk_score, "topk_score")) ||
+        (st = check_ptr(out_idx, "out_idx")) || (st = check_ptr(out_score, "out_score", false)))
+        return st;
+    if ((int64_t)shards * top_k > dsa::kMaxMergeCandidates)
+        return fail(DSA_ERR_UNSUPPORTED, "shards * top_k must be <= %d (got %lld)", dsa::kMaxMergeCandidates,
+                    (long long)shards * top_k);
+    DeviceInfo dev;
+    if ((st = device_info(&dev))) return st;
+    if (total_q == 0) return DSA_OK;
+    dsa::MergeParams p;
+    memset(&p, 0, sizeof p);
+    p.idx = topk_idx;
+    p.score = topk_score;
+    p.out_idx = out_idx;
+    p.out_score = out_score;
+    p.shards = shards;
+    p.total_q = total_q;
+    p.top_k = top_k;
+    cudaError_t e = dsa::launch_merge(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return DSA_OK;
+}
+
+dsa_status_t dsa_attn_combine(int32_t shards, int32_t total_q, int32_t heads, int32_t v_dim, const void* out_parts,
+                              const float* lse_parts, void* out, float* lse, void* stream) {
+    g_last_error.clear();
+    if (shards < 1 || total_q < 0 || heads < 1 || v_dim < 2 || (v_dim & 1))
+        return fail(DSA_ERR_INVALID_ARG, "need shards >= 1, total_q >= 0, heads >= 1 and an even v_dim >= 2 "
+                    "(got %d, %d, %d, %d)", shards, total_q, heads, v_dim);
+    dsa_status_t st;
+    if ((st = check_ptr(out_parts, "out_parts")) || (st = check_ptr(lse_parts, "lse_parts")) ||
+        (st = check_ptr(out, "out")) || (st = check_ptr(lse, "lse", false)))
+        return st;
+    DeviceInfo dev;
+    if ((st = device_info(&dev))) return st;
+    if (total_q == 0) return DSA_OK;
+    dsa::CombineParams p;
+    memset(&p, 0, sizeof p);
+    p.out_in = static_cast<const uint16_t*>(out_parts);
+    p.lse_in = lse_parts;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.shards = shards;
+    p.total_q = total_q;
+    p.heads = heads;
+    p.v_dim = v_dim;
+    cudaError_t e = dsa::launch_combine(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return DSA_OK;
+}
+
+uint64_t dsa_set_wait_limit_ns(uint64_t limit_ns) {
+    return g_wait_limit_ns.exchange(limit_ns == 0 ? 1000000000ull : limit_ns);
 }
 
 dsa_status_t dsa_append_rows(const dsa_dims_t* d, const void* k_new, const void* kv_new, const int32_t* page_table,
@@ -485,7 +607,7 @@ dsa_status_t dsa_fused_decode(const dsa_dims_t* dims, const void* q_idx, const v
     dsa::SfaLaunch SL;
     bool li = false, ls = false;
     dsa_status_t st = prepare_indexer(dims, q_idx, q_scale, w, k_cache, k_scale, page_table, seq_lens, cu_q_lens,
-                                      topk_idx, workspace, &IL, &li);
+                                      topk_idx, nullptr, workspace, &IL, &li);
     if (st) return st;
     st = prepare_sfa(dims, q, kv_cache, page_table, seq_lens, cu_q_lens, topk_idx, out, lse, workspace, &SL, &ls);
     if (st) return st;

@@ -24,7 +24,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second: the default limit, and that of every drain
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,14 +61,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Gives up after kWaitLimitNs, sets
-// DSA_DEVERR_TIMEOUT and returns false; the caller then abandons its pipeline role.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+// Waits for the phase with the given parity to complete.  Gives up after limit_ns, sets
+// DSA_DEVERR_TIMEOUT and returns false; the caller then abandons its pipeline role.  Pipeline waits pass
+// the launch's limit; the drains that must see every issued copy land before shared or tensor memory is
+// reused or released keep the default.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             raise_error(err, DSA_DEVERR_TIMEOUT);
             return false;
         }
@@ -390,6 +393,10 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     uint32_t u = __float_as_uint(f);
     if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The score a key was made from (-0 comes back as +0).
+__device__ __forceinline__ float key_score(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 }  // namespace dsa

@@ -115,6 +115,7 @@ struct CtrlSmem {
     uint64_t bfull[2];   // MX: a dequantised K tile is ready (converter warps)
     uint64_t bempty[2];  // MX: its MMAs are done
     uint64_t qbar;
+    uint64_t mma_done;   // every MMA the issuer made has completed (before tensor memory is released)
     uint32_t tmem_base;
     int32_t consumed;  // tiles consumed by the MMA warp (drain bookkeeping)
     int32_t issued;    // tiles issued by the producer
@@ -275,7 +276,8 @@ __device__ void exchange_pass(const uint32_t* keys, int n, uint32_t prefix, int 
 template <int NT>
 __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint32_t* allh, uint32_t* sbuf, int n,
                                int K, int64_t visible, int32_t* out_row, int range_start, uint32_t rank, uint32_t C,
-                               SelectSmem& S, const int32_t* pages, int32_t* rows_row) {
+                               SelectSmem& S, const int32_t* pages, int32_t* rows_row, float* score_row,
+                               int pos_begin) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // physical cache row of local key i (its page from this CTA's page list), -1 for a missing page
     auto row_of = [&](int i) -> int32_t {
@@ -283,11 +285,14 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         return pg >= 0 ? pg * kPage + (i & (kPage - 1)) : -1;
     };
     if (visible <= K) {
-        // every visible position is kept: 0..p in order (each CTA writes those of its own range), then -1
-        const int64_t own_hi = min((int64_t)range_start + n, visible);
+        // every visible position is kept: pos_begin..pos_begin+visible-1 in order (each CTA writes those of
+        // its own range), then -1
+        const int64_t own_hi = min((int64_t)range_start + n, (int64_t)pos_begin + visible);
         for (int64_t s = (int64_t)range_start + tid; s < own_hi; s += NT) {
-            out_row[s] = (int32_t)s;
-            if (rows_row) rows_row[s] = row_of((int)(s - range_start));
+            const int64_t o = s - pos_begin;
+            out_row[o] = (int32_t)s;
+            if (rows_row) rows_row[o] = row_of((int)(s - range_start));
+            if (score_row) score_row[o] = key_score(keys[s - range_start]);
         }
         const int pad = K - (int)visible;
         const int per = (pad + (int)C - 1) / (int)C;
@@ -295,6 +300,7 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         for (int s = lo + tid; s < hi; s += NT) {
             out_row[s] = -1;
             if (rows_row) rows_row[s] = -1;
+            if (score_row) score_row[s] = -INFINITY;
         }
         return;
     }
@@ -628,6 +634,7 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
                 if (pos < (uint32_t)K) {
                     out_row[pos] = range_start + i + e;
                     if (rows_row) rows_row[pos] = row_of(i + e);
+                    if (score_row) score_row[pos] = key_score(kv[e]);
                 }
                 ++pos;
             }
@@ -694,9 +701,10 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     const int nq = min(p.qb, n_b - j0);
     const int t0 = cu0 + j0;
     const int64_t p_last = (int64_t)L - n_b + j0 + nq - 1;  // position of the block's last query
-    const int range_start = (int)rank * p.chunk;
+    // this CTA's positions: its chunk of the candidate range [pos_begin, pos_end), up to the block's last query
+    const int range_start = p.pos_begin + (int)rank * p.chunk;
     const int64_t range_end = (int64_t)range_start + p.chunk;
-    const int64_t hi = range_end < p_last + 1 ? range_end : p_last + 1;
+    const int64_t hi = min(min(range_end, p_last + 1), (int64_t)p.pos_end);
     const int n_pos = hi > range_start ? (int)(hi - range_start) : 0;
     const int ntiles = (n_pos + kTileM - 1) / kTileM;
     const int n_keys = ntiles * kTileM;
@@ -753,6 +761,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             mbar_init(&ctl->tempty[i], 4);  // one arrival per warp of the epilogue group that reads it
         }
         mbar_init(&ctl->qbar, 1);
+        mbar_init(&ctl->mma_done, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->bfull[i], 4);  // MX: one arrival per converter warp
             mbar_init(&ctl->bempty[i], 1);
@@ -793,7 +802,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             int s = 0;  // ring slot and its phase, advanced without a division by the runtime depth
             uint32_t ph = 0;
             for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->empty[s], ph ^ 1u, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->empty[s], ph ^ 1u, p.err, p.wait_ns))) break;
                 if (lane == 0) {
                     const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
                     const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) *
@@ -832,17 +841,18 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             const uint32_t tmem = ctl->tmem_base;
             const uint32_t q_base = smem_u32(q_tile);
             int consumed = 0;
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err));
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err, p.wait_ns));
             if (lane == 0) ctl->qwaited = ok ? 1 : 0;
             int s = 0;
             uint32_t ph = 0;
             for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
                 const int ab = i % Cfg::kAccBufs;
                 const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err, p.wait_ns))) break;
                 // the tile to score: the loaded stage, or (MX) its dequantised copy in TMEM
                 uint64_t* ready = MX ? &ctl->bfull[i & 1] : &ctl->full[s];
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err, p.wait_ns)))
+                    break;
                 consumed = i + 1;
                 tc_fence_after();
                 if (lane == 0) {
@@ -867,6 +877,13 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 __syncwarp();
             }
             if (lane == 0 && !MX) ctl->consumed = consumed;
+            // Drain: tensor memory is released below only once every MMA issued here has completed (the
+            // epilogue has waited for all of them unless a pipeline wait gave up)
+            if (lane == 0 && consumed > 0) {
+                umma_commit(&ctl->mma_done);
+                mbar_wait(&ctl->mma_done, 0, p.err);
+            }
+            __syncwarp();
         } else if (MX && warp >= 6 && warp < 10) {
             // MX converters: each landed FP8 tile, dequantised to bf16 with the key's group scales, goes to
             // one of two TMEM tiles the MMA reads as its A operand; the FP8 stage is then free again
@@ -910,9 +927,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 tmem_st16_u32(dst + 32 * h + 16, o + 16);
             };
             for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->full[s], ph, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->full[s], ph, p.err, p.wait_ns))) break;
                 consumed = i + 1;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->bempty[i & 1], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait(&ctl->bempty[i & 1], (((uint32_t)i >> 1) & 1u) ^ 1u, p.err, p.wait_ns)))
+                    break;
                 tc_fence_after();  // the MMAs that read this TMEM tile have completed
                 const uint32_t src = smem_u32(a_tiles + (size_t)s * Cfg::kStageBytes) + row * 128;
                 const uint32_t dst = trow + (uint32_t)((i & 1) * Cfg::kACols);
@@ -956,7 +975,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 const int32_t pg = pages_s[2 * i + (row >> 6)];
                 float ksc = 1.f;
                 if (FP8 && !MX && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err, p.wait_ns))) break;
                 tc_fence_after();
                 float acc[QB];
 #pragma unroll
@@ -1020,7 +1039,8 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
 #pragma unroll
                 for (int q = 0; q < QB; ++q) {
                     uint32_t key = 0;
-                    if (q < nq && pg >= 0 && (int64_t)pos <= pq[q]) key = score_key((FP8 && !MX) ? acc[q] * ksc : acc[q]);
+                    if (q < nq && pg >= 0 && (int64_t)pos <= pq[q] && pos < p.pos_end)
+                        key = score_key((FP8 && !MX) ? acc[q] * ksc : acc[q]);
                     keys[q * p.chunk + local] = key;
                     // top-byte histogram for the first radix pass (warp-aggregated)
                     const uint32_t bin = key >> 24;
@@ -1044,12 +1064,14 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
 
     // ---- cluster-wide Top-K per query -------------------------------------------------------------------
     for (int q = 0; q < nq; ++q) {
-        const int64_t visible = (int64_t)L - n_b + j0 + q + 1;
+        // candidate positions of this query: [pos_begin, min(p + 1, pos_end))
+        const int64_t visible = max((int64_t)0, min((int64_t)L - n_b + j0 + q + 1, (int64_t)p.pos_end) - p.pos_begin);
         // the smem stage ring is idle once every CTA has scored: it holds the select's fallback exchange space
         cluster_select<NT>(keys + (size_t)q * p.chunk, hist0 + q * 256, allh, reinterpret_cast<uint32_t*>(a_tiles),
                        n_keys, p.top_k, visible,
                        p.topk + (int64_t)(t0 + q) * p.top_k, range_start, rank, C, *sel, pages_s,
-                       p.rows_out ? p.rows_out + (int64_t)(t0 + q) * p.top_k : nullptr);
+                       p.rows_out ? p.rows_out + (int64_t)(t0 + q) * p.top_k : nullptr,
+                       p.topk_score ? p.topk_score + (int64_t)(t0 + q) * p.top_k : nullptr, p.pos_begin);
     }
     // No cluster barrier here: every remote access is a histogram push, and the pushes of a pass complete
     // before that pass's barrier, so after the last pass no CTA touches another's shared memory.
@@ -1064,6 +1086,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             mbar_inval(&ctl->tempty[i]);
         }
         mbar_inval(&ctl->qbar);
+        mbar_inval(&ctl->mma_done);
         for (int i = 0; i < 2; ++i) {
             mbar_inval(&ctl->bfull[i]);
             mbar_inval(&ctl->bempty[i]);

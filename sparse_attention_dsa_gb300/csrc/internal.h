@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dsa.h"
+
 namespace dsa {
 
 constexpr int kMaxStages = 8;
@@ -30,6 +32,10 @@ struct IndexerParams {
     int32_t stages;          // filled in by the launcher
     int32_t* rows_out;       // [T, K] physical cache row of every selected position (-1 for padding), or null
     const void* q_idx_codes;  // MXFP8: the q_idx codes [T, Hi, Di] (dequantised at set-up instead of loaded by TMA)
+    float* topk_score;        // [T, K] fp32 score of every selected position (-inf for padding), or null
+    int32_t pos_begin;        // only positions in [pos_begin, pos_end) are candidates (pos_begin % 64 == 0)
+    int32_t pos_end;
+    uint64_t wait_ns;         // limit of every pipeline wait (drains keep the default limit)
 };
 
 struct IndexerLaunch {
@@ -78,6 +84,9 @@ struct SfaParams {
     int32_t kv_fp8;       // kv_cache rows are in the FP8 row layout
     const int32_t* rows_in;  // [T, K] physical rows of topk written by the indexer phase in the same launch, or null
     int32_t one_query_per_seq;  // every sequence has exactly one query token: token t belongs to sequence t
+    int32_t pos_begin;          // Top-K entries outside [pos_begin, pos_end) are skipped (a context shard)
+    int32_t pos_end;
+    uint64_t wait_ns;           // limit of every pipeline wait (drains keep the default limit)
 };
 
 struct SfaLaunch {
@@ -138,7 +147,46 @@ size_t sfa_merge_ctas(int64_t total_q, int32_t top_k);
 // Bytes of workspace the library uses: the 256-byte error word area, plus the attention merge scratch.
 constexpr size_t kErrorWordArea = 256;
 
+// ---- context-parallel decode: merge of shard Top-K lists, combine of shard attention outputs -----------
+struct MergeParams {
+    const int32_t* idx;   // [shards, T, K] shard-local selections (positions, -1 padded)
+    const float* score;   // [shards, T, K] their scores
+    int32_t* out_idx;     // [T, K]
+    float* out_score;     // [T, K] or null
+    int32_t shards;
+    int32_t total_q;
+    int32_t top_k;
+};
+size_t merge_smem_bytes(int shards, int top_k);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+struct CombineParams {
+    const uint16_t* out_in;  // [shards, T, Hq, Dv] bf16 bits
+    const float* lse_in;     // [shards, T, Hq]
+    uint16_t* out;           // [T, Hq, Dv] bf16 bits
+    float* lse;              // [T, Hq] or null
+    int32_t shards;
+    int32_t total_q;
+    int32_t heads;
+    int32_t v_dim;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
 // Sets the message returned by dsa_last_error_message() on this host thread.
 void set_last_error(const char* message);
+
+// Limit of the kernels' pipeline waits for launches made from now on (dsa_set_wait_limit_ns).
+uint64_t wait_limit_ns();
+
+// The host half of dsa_indexer_topk: every argument check and the launch plan, nothing enqueued (*launch
+// is false when there is nothing to launch); then the launch itself.
+dsa_status_t prepare_indexer_call(const dsa_dims_t* dims, const void* q_idx, const void* q_scale, const float* w,
+                                  const void* k_cache, const void* k_scale, const int32_t* page_table,
+                                  const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t* topk_idx,
+                                  float* topk_score, void* workspace, IndexerLaunch* launch_out, bool* launch);
+dsa_status_t launch_indexer_call(const IndexerLaunch& launch, void* stream);
+
+// Candidates one dsa_topk_merge call may hold per query token (shards * top_k): its shared-memory keys.
+constexpr int kMaxMergeCandidates = 16384;
 
 }  // namespace dsa

@@ -273,7 +273,9 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         const int32_t* pt_row = p.page_table + (int64_t)b * p.max_pages;
 #pragma unroll
         for (int k = 0; k < kEntPerThread; ++k)
-            pg[k] = (ent[k] >= 0 && (ent[k] >> 6) < p.max_pages) ? __ldg(pt_row + (ent[k] >> 6)) : -1;
+            pg[k] = (ent[k] >= p.pos_begin && ent[k] >= 0 && ent[k] < p.pos_end && (ent[k] >> 6) < p.max_pages)
+                        ? __ldg(pt_row + (ent[k] >> 6))
+                        : -1;
     }
 #pragma unroll
     for (int k = 0; k < kEntPerThread; ++k) {
@@ -281,7 +283,8 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         if (e >= ntiles * kRows) continue;
         int32_t row = -1;
         const int32_t s_pos = ent[k];
-        if (s_pos >= 0) {
+        // entries of another context shard are skipped (valid, not this call's)
+        if (s_pos >= 0 && s_pos >= p.pos_begin && s_pos < p.pos_end) {
             if ((int64_t)s_pos > pos) {
                 if (dvh == 0) raise_error(p.err, DSA_DEVERR_INDEX);
             } else if (pg[k] < 0 || pg[k] >= p.num_pages) {
@@ -336,7 +339,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 const int bsel = i & 1;
                 uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
                 uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err, p.wait_ns))) break;
                 const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -363,7 +366,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 const int bsel = i & 1;
                 uint64_t* full = v_part ? &ctl->v_full[bsel] : &ctl->k_full[bsel];
                 uint64_t* empty = v_part ? &ctl->v_empty[bsel] : &ctl->k_empty[bsel];
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err))) break;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty, (((uint32_t)i >> 1) & 1u) ^ 1u, p.err, p.wait_ns))) break;
                 const uint32_t base = smem_u32(v_part ? vbuf + bsel * kVBufBytes : kbuf + bsel * kKBufBytes);
     #pragma unroll 1
                 for (int r0 = 4 * pw; r0 < kRows; r0 += 4 * nw) {
@@ -390,12 +393,12 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
     else if (warp == 1) {
         // ---------------- MMA issuer: S(i) = Q K(i)^T, then O += P(i-1) V(i-1) ----------------
         if (lane == 0) {
-            bool ok = mbar_wait(&ctl->q_full, 0, p.err);
+            bool ok = mbar_wait(&ctl->q_full, 0, p.err, p.wait_ns);
             ctl->q_waited = ok ? 1 : 0;
-            ok = ok && mbar_wait(&ctl->qt_full, 0, p.err);
+            ok = ok && mbar_wait(&ctl->qt_full, 0, p.err, p.wait_ns);
             const uint32_t q_base = smem_u32(q_s), kb = smem_u32(kbuf), vb = smem_u32(vbuf);
             auto pv = [&](int j) -> bool {
-                if (!mbar_wait(&ctl->p_full, (uint32_t)j & 1u, p.err)) return false;
+                if (!mbar_wait(&ctl->p_full, (uint32_t)j & 1u, p.err, p.wait_ns)) return false;
                 tc_fence_after();
                 const uint32_t vbase = vb + (j & 1) * kVBufBytes;
 #pragma unroll
@@ -431,8 +434,8 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             for (int i = 0; ok && i < ntiles; ++i) {
                 const uint32_t ph = ((uint32_t)i >> 1) & 1u;
                 // K part of S(i): needs its rows and the softmax to have read S(i-1)
-                if (!mbar_wait(&ctl->k_full[i & 1], ph, p.err) ||
-                    !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err)) {
+                if (!mbar_wait(&ctl->k_full[i & 1], ph, p.err, p.wait_ns) ||
+                    !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -445,7 +448,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(&ctl->v_full[i & 1], ph, p.err)) {
+                if (!mbar_wait(&ctl->v_full[i & 1], ph, p.err, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -455,6 +458,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 umma_commit(&ctl->s_full);
             }
             if (ok && ntiles > 0) pv(ntiles - 1);
+            // drain (default limit): every MMA has completed before tensor memory is read back or released
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, p.err);
         }
@@ -465,7 +469,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         for (int i = 0; i < ntiles; ++i) {
             const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
             const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + 32 + lane] >= 0);
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full, (uint32_t)i & 1u, p.err))) break;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full, (uint32_t)i & 1u, p.err, p.wait_ns))) break;
             tc_fence_after();
             float sv[kRows];
             {
@@ -522,7 +526,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             }
             const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             // P(i-1) V(i-1) has completed: the P columns are free and O is stable
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err))) break;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err, p.wait_ns))) break;
             tc_fence_after();
             if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll 1
@@ -545,7 +549,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->p_full);
         }
-        if (ntiles > 0) mbar_wait(&ctl->p_empty, ((uint32_t)(ntiles - 1)) & 1u, p.err);
+        if (ntiles > 0) mbar_wait(&ctl->p_empty, ((uint32_t)(ntiles - 1)) & 1u, p.err, p.wait_ns);
         tc_fence_after();
     }
     tc_fence_before();
@@ -676,7 +680,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 w_oth *= inv;
                 if (part == 0 && own_row && dvh == 0 && p.lse)
                     p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-                const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->merge_full, 0, p.err));
+                const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->merge_full, 0, p.err, p.wait_ns));
                 const int c_lo = part == 0 ? 0 : (part == 1 ? 6 : 11), c_hi = part == 0 ? 6 : (part == 1 ? 11 : 16);
                 const uint32_t rowp = smem_u32(obuf) + (uint32_t)(jo * slice + r) * 1024u;
 #pragma unroll 1
@@ -739,7 +743,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 }
                 if (part == 0 && own_row && dvh == 0 && p.lse)
                     p.lse[(int64_t)t * p.heads + hh] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-                const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->merge_full, 0, p.err));
+                const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->merge_full, 0, p.err, p.wait_ns));
                 const int c_lo = part == 0 ? 0 : (part == 1 ? 6 : 11), c_hi = part == 0 ? 6 : (part == 1 ? 11 : 16);
 #pragma unroll 1
                 for (int c = c_lo; c < c_hi; ++c) {
@@ -778,8 +782,8 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                 }
             }
         }
-        // every bulk copy into this CTA has landed before it exits (the combining warps saw the barrier;
-        // a CTA without owned rows waits here)
+        // drain (default limit): every bulk copy into this CTA has landed before it exits (the combining
+        // warps saw the barrier unless their wait gave up; a CTA without owned rows waits here)
         if (tid == 0) mbar_wait(&ctl->merge_full, 0, p.err);
     }
     tc_fence_before();

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert dsa.abi_version() == 3
+    assert dsa.abi_version() == 4
     for s in range(6):
         assert dsa.status_string(s).startswith("DSA_")
     assert "unknown" in dsa.status_string(99)
@@ -72,11 +72,29 @@ FAKE = 0x10000  # an aligned non-null value; validation rejects the call before 
 
 def _indexer(d, **ptrs):
     p = dict(q_idx=FAKE, q_scale=None, w=FAKE, k_cache=FAKE, k_scale=None, page_table=FAKE, seq_lens=FAKE,
-             cu_q_lens=FAKE, topk=FAKE, ws=FAKE)
+             cu_q_lens=FAKE, topk=FAKE, score=None, ws=FAKE)
     p.update(ptrs)
     return dsa.lib().dsa_indexer_topk(ctypes.byref(d) if d is not None else None, p["q_idx"], p["q_scale"], p["w"],
                                       p["k_cache"], p["k_scale"], p["page_table"], p["seq_lens"], p["cu_q_lens"],
-                                      p["topk"], p["ws"], None)
+                                      p["topk"], p["score"], p["ws"], None)
+
+
+def _indexer_shard(d, begin, end, **ptrs):
+    p = dict(q_idx=FAKE, q_scale=None, w=FAKE, k_cache=FAKE, k_scale=None, page_table=FAKE, seq_lens=FAKE,
+             cu_q_lens=FAKE, topk=FAKE, score=FAKE, ws=FAKE)
+    p.update(ptrs)
+    return dsa.lib().dsa_indexer_topk_shard(ctypes.byref(d), p["q_idx"], p["q_scale"], p["w"], p["k_cache"],
+                                            p["k_scale"], p["page_table"], p["seq_lens"], p["cu_q_lens"], begin, end,
+                                            p["topk"], p["score"], p["ws"], None)
+
+
+def _static(d, **ptrs):
+    p = dict(q_idx=FAKE, q_scale=None, w=FAKE, k_cache=FAKE, k_scale=None, page_table=FAKE, seq_lens=FAKE,
+             cu_q_lens=FAKE, topk=FAKE, score=None, err=None)
+    p.update(ptrs)
+    return dsa.lib().dsa_indexer_topk_static(ctypes.byref(d) if d is not None else None, p["q_idx"], p["q_scale"],
+                                             p["w"], p["k_cache"], p["k_scale"], p["page_table"], p["seq_lens"],
+                                             p["cu_q_lens"], p["topk"], p["score"], p["err"], None)
 
 
 def _sfa(d, **ptrs):
@@ -160,6 +178,49 @@ def test_append_rejects_bad_arguments(L):
     # a NULL new-row pointer skips that cache (and its checks); nothing to do returns before any launch
     assert _append(_dims(), k_new=None, kv_new=None, k_cache=None, kv_cache=None) == dsa.DSA_OK
     assert _append(_dims(total_q=0)) == dsa.DSA_OK
+
+
+def test_indexer_topk_score_pointer_is_checked(L):
+    assert _indexer(_dims(), score=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG and "topk_score" in _msg()
+
+
+@pytest.mark.parametrize("begin,end", [(-64, 128), (32, 4096), (128, 128), (256, 64)])
+def test_indexer_shard_rejects_bad_ranges(L, begin, end):
+    assert _indexer_shard(_dims(), begin, end) == dsa.DSA_ERR_INVALID_ARG and "range" in _msg()
+
+
+def test_sfa_shard_rejects_bad_ranges(L):
+    def call(begin, end):
+        return L.dsa_sparse_attn_shard(ctypes.byref(_dims()), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, begin, end, FAKE,
+                                       None, FAKE, None)
+    assert call(-1, 10) == dsa.DSA_ERR_INVALID_ARG and "range" in _msg()
+    assert call(64, 64) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_merge_and_combine_validate(L):
+    assert L.dsa_topk_merge(0, 4, 16, FAKE, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_topk_merge(2, 4, 16, FAKE, None, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG and "score" in _msg()
+    assert L.dsa_topk_merge(2, 4, 16, FAKE, FAKE, FAKE + 4, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_topk_merge(8, 4, 4096, FAKE, FAKE, FAKE, None, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_attn_combine(2, 4, 128, 511, FAKE, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_attn_combine(0, 4, 128, 512, FAKE, FAKE, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_attn_combine(2, 4, 128, 512, FAKE, FAKE, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_static_entry_rejects_before_touching_the_device(L):
+    """The allocation-free indexer checks its host arguments before it looks anything up or enqueues: a NULL
+    dims and a misaligned device_error pointer are rejected with no device at all."""
+    assert _static(None) == dsa.DSA_ERR_INVALID_ARG and "dims" in _msg()
+    assert _static(_dims(), err=FAKE + 2) == dsa.DSA_ERR_INVALID_ARG and "device_error" in _msg()
+
+
+def test_wait_limit_setter_round_trips(L):
+    old = dsa.set_wait_limit_ns(1234)
+    try:
+        assert dsa.set_wait_limit_ns(0) == 1234  # 0 restores the default of one second
+        assert dsa.set_wait_limit_ns(old) == 10 ** 9
+    finally:
+        dsa.set_wait_limit_ns(old)
 
 
 def test_device_error_helpers_validate(L):
