@@ -41,6 +41,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -392,71 +394,96 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
     }
     else if (warp == 1) {
         // ---------------- MMA issuer: S(i) = Q K(i)^T, then O += P(i-1) V(i-1) ----------------
+        // One thread issues every MMA, so its issue path is kept short: each shared-memory descriptor is a
+        // precomputed base plus a constant offset (the start address field holds address / 16 and no address
+        // here reaches 2^18, so adding to the descriptor adds to the address), and the atom order of each
+        // value half is a compile-time list.
         if (lane == 0) {
             bool ok = mbar_wait(&ctl->q_full, 0, p.err, p.wait_ns);
             ctl->q_waited = ok ? 1 : 0;
             ok = ok && mbar_wait(&ctl->qt_full, 0, p.err, p.wait_ns);
-            const uint32_t q_base = smem_u32(q_s), kb = smem_u32(kbuf), vb = smem_u32(vbuf);
+            const uint64_t qd0 = smem_desc(smem_u32(q_s), 16, 1024, kSwizzle128B);   // Q atom a: + a * (kQAtomBytes / 16)
+            const uint64_t kd0 = smem_desc(smem_u32(kbuf), 16, 1024, kSwizzle128B);  // K part buffer, slot
+            const uint64_t vd0 = smem_desc(smem_u32(vbuf), 16, 1024, kSwizzle128B);  // V part buffer, slot
+            // the V part as an MN-major operand of P V: 64-dim atoms kAtomBytes apart, 8-row groups 1024 B apart
+            const uint64_t pvd0 = smem_desc(smem_u32(vbuf), kAtomBytes, 1024, kSwizzle128B);
+            constexpr uint32_t kAtomStep = kAtomBytes / 16, kKBufStep = kKBufBytes / 16, kVBufStep = kVBufBytes / 16;
             auto pv = [&](int j) -> bool {
                 if (!mbar_wait(&ctl->p_full, (uint32_t)j & 1u, p.err, p.wait_ns)) return false;
                 tc_fence_after();
-                const uint32_t vbase = vb + (j & 1) * kVBufBytes;
+                const uint64_t bd = pvd0 + (uint64_t)((j & 1) * kVBufStep);
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk) {
-                    // V part as an MN-major operand: 64-dim atoms kAtomBytes apart, 8-row groups 1024 B apart
-                    const uint64_t bd = smem_desc(vbase + kk * 2048, kAtomBytes, 1024, kSwizzle128B);
-                    umma_f16_ts(tmem, tmem + kPCol + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_f16_ts(tmem, tmem + kPCol + kk * 8, bd + (uint64_t)(kk * 128), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&ctl->v_empty[j & 1]);
                 umma_commit(&ctl->p_empty);
                 return true;
             };
-            // S(i) over the atoms of one part (the K part first: it starts the accumulation)
-            auto qk = [&](int i, bool v_atoms) {
-                const uint32_t kbase = kb + (i & 1) * kKBufBytes, vbase = vb + (i & 1) * kVBufBytes;
+            // S += Q atom A . (the part's slot at descriptor bd), K = 64 dims as four MMAs of K = 16
+            auto qk_atom = [&](auto a_c, uint64_t bd, bool first) {
+                constexpr int A = decltype(a_c)::value;
 #pragma unroll
-                for (int a = 0; a < kAtoms; ++a) {
-                    if (is_v_atom(a, dvh) != v_atoms) continue;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t boff = part_slot(a, dvh) * kAtomBytes + kk * 32;
-                        const uint64_t bd = smem_desc((v_atoms ? vbase : kbase) + boff, 16, 1024, kSwizzle128B);
-                        const uint32_t acc = (v_atoms || part_slot(a, dvh) != 0 || kk != 0) ? 1u : 0u;
-                        if (a < kSmemQAtoms) {
-                            const uint64_t ad = smem_desc(q_base + a * kQAtomBytes + kk * 32, 16, 1024, kSwizzle128B);
-                            umma_f16_ss(tmem + kSCol, ad, bd, kIdescQK, acc);
-                        } else {
-                            umma_f16_ts(tmem + kSCol, tmem + kQCol + (a - kSmemQAtoms) * 32 + kk * 8, bd, kIdescQK, acc);
-                        }
-                    }
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                    if constexpr (A < kSmemQAtoms)
+                        umma_f16_ss(tmem + kSCol, qd0 + (uint64_t)(A * (kQAtomBytes / 16) + 2 * kk), bd + 2 * kk, kIdescQK, acc);
+                    else
+                        umma_f16_ts(tmem + kSCol, tmem + kQCol + (A - kSmemQAtoms) * 32 + kk * 8, bd + 2 * kk, kIdescQK, acc);
                 }
             };
-            for (int i = 0; ok && i < ntiles; ++i) {
-                const uint32_t ph = ((uint32_t)i >> 1) & 1u;
-                // K part of S(i): needs its rows and the softmax to have read S(i-1)
-                if (!mbar_wait(&ctl->k_full[i & 1], ph, p.err, p.wait_ns) ||
-                    !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err, p.wait_ns)) {
-                    ok = false;
-                    break;
+            auto main_loop = [&](auto dvh_c) {
+                constexpr int DVH = decltype(dvh_c)::value;
+                // K part (slots 0-4): the other value half's four latent atoms, then the rotary atom; V part
+                // (slots 0-3): this half's four latent atoms
+                using K0 = std::integral_constant<int, DVH == 0 ? 4 : 0>;
+                using K1 = std::integral_constant<int, DVH == 0 ? 5 : 1>;
+                using K2 = std::integral_constant<int, DVH == 0 ? 6 : 2>;
+                using K3 = std::integral_constant<int, DVH == 0 ? 7 : 3>;
+                using K4 = std::integral_constant<int, kAtoms - 1>;
+                using V0 = std::integral_constant<int, 4 * DVH>;
+                using V1 = std::integral_constant<int, 4 * DVH + 1>;
+                using V2 = std::integral_constant<int, 4 * DVH + 2>;
+                using V3 = std::integral_constant<int, 4 * DVH + 3>;
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const uint32_t ph = ((uint32_t)i >> 1) & 1u;
+                    // K part of S(i): needs its rows and the softmax to have read S(i-1)
+                    if (!mbar_wait(&ctl->k_full[i & 1], ph, p.err, p.wait_ns) ||
+                        !mbar_wait(&ctl->s_empty, ((uint32_t)i & 1u) ^ 1u, p.err, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // the rows were written by cp.async (generic proxy); the MMAs read them through the async proxy
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const uint64_t kd = kd0 + (uint64_t)((i & 1) * kKBufStep);
+                    qk_atom(K0{}, kd, true);
+                    qk_atom(K1{}, kd + kAtomStep, false);
+                    qk_atom(K2{}, kd + 2 * kAtomStep, false);
+                    qk_atom(K3{}, kd + 3 * kAtomStep, false);
+                    qk_atom(K4{}, kd + 4 * kAtomStep, false);
+                    umma_commit(&ctl->k_empty[i & 1]);
+                    if (i > 0 && !pv(i - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&ctl->v_full[i & 1], ph, p.err, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const uint64_t vd = vd0 + (uint64_t)((i & 1) * kVBufStep);
+                    qk_atom(V0{}, vd, false);
+                    qk_atom(V1{}, vd + kAtomStep, false);
+                    qk_atom(V2{}, vd + 2 * kAtomStep, false);
+                    qk_atom(V3{}, vd + 3 * kAtomStep, false);
+                    umma_commit(&ctl->s_full);
                 }
-                // the rows were written by cp.async (generic proxy); the MMAs read them through the async proxy
-                fence_proxy_async_smem();
-                tc_fence_after();
-                qk(i, false);
-                umma_commit(&ctl->k_empty[i & 1]);
-                if (i > 0 && !pv(i - 1)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(&ctl->v_full[i & 1], ph, p.err, p.wait_ns)) {
-                    ok = false;
-                    break;
-                }
-                fence_proxy_async_smem();
-                tc_fence_after();
-                qk(i, true);
-                umma_commit(&ctl->s_full);
-            }
+            };
+            if (dvh == 0)
+                main_loop(std::integral_constant<int, 0>{});
+            else
+                main_loop(std::integral_constant<int, 1>{});
             if (ok && ntiles > 0) pv(ntiles - 1);
             // drain (default limit): every MMA has completed before tensor memory is read back or released
             umma_commit(&ctl->mma_done);
