@@ -656,6 +656,10 @@ template <int HI, int DI, int QB, bool FP8, int NT, bool LAST_TMEM, bool MX = fa
 __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p,
                                             uint8_t* smem_raw) {
     using Cfg = IdxCfg<HI, DI, QB, FP8, MX>;
+    // four queries of 64 heads per block (two accumulator buffers): both epilogue groups read every tile,
+    // two queries each
+    constexpr bool kSplitQueries = !MX && QB == 4 && Cfg::kAccBufs == 2;
+    static_assert(!kSplitQueries || HI % 32 == 0, "split epilogue: the 32-column head loop");
     static_assert(NT % 32 == 0 && NT >= 256 && NT / 32 <= kMaxWarps, "thread count of the indexer body");
     // 1024-byte alignment for the swizzled operand tiles, by pointer arithmetic on the shared array (an
     // integer round trip would hide from the compiler that the derived pointers are shared, turning every
@@ -758,7 +762,8 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
-            mbar_init(&ctl->tempty[i], 4);  // one arrival per warp of the epilogue group that reads it
+            // one arrival per epilogue warp that reads it: one group, or both groups with split queries
+            mbar_init(&ctl->tempty[i], kSplitQueries ? 8 : 4);
         }
         mbar_init(&ctl->qbar, 1);
         mbar_init(&ctl->mma_done, 1);
@@ -843,6 +848,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             int consumed = 0;
             bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err, p.wait_ns));
             if (lane == 0) ctl->qwaited = ok ? 1 : 0;
+            // Precomputed descriptors: one thread issues every MMA, so each descriptor is a base plus a
+            // compile-time offset (the start address field holds address / 16 and no address here reaches
+            // 2^18, so adding to the descriptor adds to the address).
+            const uint64_t ad0 = smem_desc(smem_u32(a_tiles), 16, 1024, kSwizzle128B);  // stage s: + s * kStageBytes / 16
+            const uint64_t bd0 = smem_desc(q_base, 16, 1024, kSwizzle128B);
             int s = 0;
             uint32_t ph = 0;
             for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
@@ -856,13 +866,14 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 consumed = i + 1;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t a_base = smem_u32(a_tiles + (size_t)s * Cfg::kStageBytes);
+                    const uint64_t ads = ad0 + (uint64_t)((uint32_t)s * (uint32_t)(Cfg::kStageBytes / 16));
 #pragma unroll
                     for (int k = 0; k < Cfg::kKSteps; ++k) {
-                        const int kb = k * Cfg::kMmaK * Cfg::kMmaElem;  // byte offset along K
+                        constexpr int kStep = Cfg::kMmaK * Cfg::kMmaElem;  // bytes along K per MMA
+                        const int kb = k * kStep;
                         const int atom = kb / 128, off = kb % 128;
-                        const uint64_t ad = smem_desc(a_base + atom * (kTileM * 128) + off, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(q_base + atom * (Cfg::kN * 128) + off, 16, 1024, kSwizzle128B);
+                        const uint64_t ad = ads + (uint64_t)((atom * (kTileM * 128) + off) / 16);
+                        const uint64_t bd = bd0 + (uint64_t)((atom * (Cfg::kN * 128) + off) / 16);
                         if (MX)
                             umma_f16_ts(tmem + ab * Cfg::kN, tmem + Cfg::kACol + (i & 1) * Cfg::kACols + k * 8, bd,
                                         Cfg::kIdesc, k > 0);
@@ -956,9 +967,12 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             }
             if (lane == 0 && warp == 6) ctl->consumed = consumed;
         } else if (warp >= 2 && warp < (MX ? 6 : 10)) {
-            // Two epilogue groups (warps 2-5 take the even tiles, warps 6-9 the odd ones; MX keeps warps
-            // 6-9 for its converters): both groups cover the four TMEM lane quadrants, and an accumulator
-            // buffer is only ever read by one group, so its release count stays four.
+            // Two epilogue groups (warps 2-5 and 6-9; MX keeps warps 6-9 for its converters), each covering
+            // the four TMEM lane quadrants.  With up to two queries per block they take alternate tiles (an
+            // accumulator buffer is read by one group).  With four queries a tile's accumulator is 256
+            // columns, only two buffers fit in tensor memory, and the MMA of tile i + 2 waits for the
+            // epilogue of tile i: both groups then read every tile, each for two of the queries, which
+            // halves the epilogue's chain of tensor-memory loads per tile.
             static_assert(MX || NT >= 320, "the second epilogue group is warps 6-9");
             const int group = (warp - 2) >> 2;
             const uint32_t quad = (uint32_t)(warp & 3);  // TMEM lanes this warp may access
@@ -967,7 +981,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             int64_t pq[QB];
 #pragma unroll
             for (int q = 0; q < QB; ++q) pq[q] = (int64_t)L - n_b + j0 + q;
-            for (int i = group; i < ntiles; i += (MX ? 1 : 2)) {
+            for (int i = kSplitQueries ? 0 : group; i < ntiles; i += (MX || kSplitQueries) ? 1 : 2) {
                 const int ab = i % Cfg::kAccBufs;
                 const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
                 const int local = i * kTileM + row;
@@ -986,6 +1000,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     // keep the FMA chains short, and the weights come four at a time.
 #pragma unroll
                     for (int q = 0; q < QB; ++q) {
+                        if (kSplitQueries && (q >> 1) != group) continue;  // the other group's queries
                         // partial sums in pairs (2k, 2k+1), advanced by the packed fp32x2 FMA: one instruction
                         // per two heads, each lane of it the same rounding as a scalar FMA
                         float2 part[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -1038,6 +1053,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 if (lane == 0) mbar_arrive(&ctl->tempty[ab]);
 #pragma unroll
                 for (int q = 0; q < QB; ++q) {
+                    if (kSplitQueries && (q >> 1) != group) continue;
                     uint32_t key = 0;
                     if (q < nq && pg >= 0 && (int64_t)pos <= pq[q] && pos < p.pos_end)
                         key = score_key((FP8 && !MX) ? acc[q] * ksc : acc[q]);
