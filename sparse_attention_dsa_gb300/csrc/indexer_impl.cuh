@@ -758,7 +758,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], MX ? 4 : 1);  // MX: the four converter warps free the stage
+            mbar_init(&ctl->empty[s], MX ? 4 : 1);  // MX: the four converter warps free the stage; else the epilogue
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
@@ -882,7 +882,9 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                         else
                             umma_f8_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
                     }
-                    umma_commit(MX ? &ctl->bempty[i & 1] : &ctl->empty[s]);
+                    // MX: the converters free the FP8 stage; otherwise the epilogue frees it once it has seen
+                    // this tile's MMAs complete (one commit per tile for this thread)
+                    if (MX) umma_commit(&ctl->bempty[i & 1]);
                     umma_commit(&ctl->tfull[ab]);
                 }
                 __syncwarp();
@@ -990,6 +992,9 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 float ksc = 1.f;
                 if (FP8 && !MX && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err, p.wait_ns))) break;
+                // the tile's MMAs have completed, so its stage is free for the producer (one arrival, from the
+                // first warp of the group that owns the tile)
+                if (!MX && lane == 0 && (warp & 3) == 0 && (!kSplitQueries || group == 0)) mbar_arrive(&ctl->empty[i % S]);
                 tc_fence_after();
                 float acc[QB];
 #pragma unroll
