@@ -16,7 +16,7 @@ import sparse_attention_dsa_gb300 as dsa
 from gen import bf16_to_f32, f32_to_bf16
 from gen.workloads import config, make_workload
 
-from _gpu import DeviceWorkload, check_attention, check_topk, ensure_built
+from _gpu import DeviceWorkload, check_attention, check_topk, dims_for, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +39,10 @@ SMALL = {
     "k_equals_one": ([700, 64], [1, 1], 64, 128, False, 1, 32, {}),
     # 32 query tokens: the attention splits each token's positions in two (the two-split merge path)
     "thirty_two_tokens": ([700 + 97 * i for i in range(32)], [1] * 32, 64, 128, False, 512, 128, {}),
+    # the largest supported K (4096): one query per sequence (single launch), and FP8 keys with two
+    # queries in a sequence (two launches); contexts below, just above and well above K
+    "k_max_decode": ([9000, 4100, 3000], [1, 1, 1], 64, 128, False, 4096, 128, {}),
+    "k_max_fp8_two_queries": ([9000, 4097], [2, 1], 64, 128, True, 4096, 128, {}),
 }
 
 
@@ -70,6 +74,22 @@ def test_attention_on_oracle_selection_in_any_order(name):
     assert dw.error_word() == 0
     out, lse = dw.out_host()
     check_attention(wl, shuffled, out, lse)
+
+
+def test_no_query_tokens_launches_nothing():
+    """total_q = 0: every compute entry point returns OK, writes nothing and sets no device error."""
+    wl = _small("hi64_bf16")
+    dw = DeviceWorkload(wl)
+    d = dims_for(wl, total_q=0)
+    dw.topk.fill_(-7)
+    dw.out.fill_(3)
+    assert dsa.fused_decode_launches(d) == 0
+    dw.fused(dims=d)
+    dw.indexer(dims=d)
+    dw.sfa(topk=dw.topk, dims=d)
+    torch.cuda.synchronize()
+    assert dw.error_word() == 0
+    assert bool((dw.topk == -7).all()) and bool((dw.out == 3).all())
 
 
 def test_attention_covering_whole_context_equals_dense():
