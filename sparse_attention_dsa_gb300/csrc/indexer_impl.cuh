@@ -659,6 +659,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     // four queries of 64 heads per block (two accumulator buffers): both epilogue groups read every tile,
     // two queries each
     constexpr bool kSplitQueries = !MX && QB == 4 && Cfg::kAccBufs == 2;
+    // Several queries per block (scoring bound by the MMA thread's loop rather than by the K-cache
+    // stream): the producer also waits until the tile's accumulator buffer is free before loading it, so
+    // the MMA thread waits only for the landed stage.  With one query the stream sets the pace, and the
+    // producer runs ahead by the full ring instead.
+    constexpr bool kProducerWaitsAcc = !MX && QB >= 2;
     static_assert(!kSplitQueries || HI % 32 == 0, "split epilogue: the 32-column head loop");
     static_assert(NT % 32 == 0 && NT >= 256 && NT / 32 <= kMaxWarps, "thread count of the indexer body");
     // 1024-byte alignment for the swizzled operand tiles, by pointer arithmetic on the shared array (an
@@ -808,6 +813,11 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             uint32_t ph = 0;
             for (int i = 0; i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->empty[s], ph ^ 1u, p.err, p.wait_ns))) break;
+                if constexpr (kProducerWaitsAcc) {
+                    const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[i % Cfg::kAccBufs], aph ^ 1u, p.err, p.wait_ns)))
+                        break;
+                }
                 if (lane == 0) {
                     const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
                     const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) *
@@ -843,29 +853,31 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             }
             if (lane == 0) ctl->issued = issued;
         } else if (warp == 1) {
-            const uint32_t tmem = ctl->tmem_base;
-            const uint32_t q_base = smem_u32(q_tile);
-            int consumed = 0;
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err, p.wait_ns));
-            if (lane == 0) ctl->qwaited = ok ? 1 : 0;
-            // Precomputed descriptors: one thread issues every MMA, so each descriptor is a base plus a
-            // compile-time offset (the start address field holds address / 16 and no address here reaches
-            // 2^18, so adding to the descriptor adds to the address).
-            const uint64_t ad0 = smem_desc(smem_u32(a_tiles), 16, 1024, kSwizzle128B);  // stage s: + s * kStageBytes / 16
-            const uint64_t bd0 = smem_desc(q_base, 16, 1024, kSwizzle128B);
-            int s = 0;
-            uint32_t ph = 0;
-            for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-                const int ab = i % Cfg::kAccBufs;
-                const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err, p.wait_ns))) break;
-                // the tile to score: the loaded stage, or (MX) its dequantised copy in TMEM
-                uint64_t* ready = MX ? &ctl->bfull[i & 1] : &ctl->full[s];
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err, p.wait_ns)))
-                    break;
-                consumed = i + 1;
-                tc_fence_after();
-                if (lane == 0) {
+            // One thread runs the issue loop (lanes 1-31 wait at the warp barrier below): the per-tile cost of
+            // this role is its own instruction stream (a barrier test, a tcgen05 fence, one issue per MMA at
+            // about 46 cycles each, one commit), so no lane votes or warp barriers are added to it.
+            if (lane == 0) {
+                const uint32_t tmem = ctl->tmem_base;
+                int consumed = 0;
+                const bool ok = mbar_wait(&ctl->qbar, 0, p.err, p.wait_ns);
+                ctl->qwaited = ok ? 1 : 0;
+                // Precomputed descriptors: each is a base plus a compile-time offset (the start address field
+                // holds address / 16 and no address here reaches 2^18, so adding to the descriptor adds to the
+                // address).
+                const uint64_t ad0 = smem_desc(smem_u32(a_tiles), 16, 1024, kSwizzle128B);  // stage s: + s * kStageBytes / 16
+                const uint64_t bd0 = smem_desc(smem_u32(q_tile), 16, 1024, kSwizzle128B);
+                int s = 0;
+                uint32_t ph = 0;
+                for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                    const int ab = i % Cfg::kAccBufs;
+                    const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
+                    // the accumulator buffer is free (seen here, or by the producer before it loaded the stage)
+                    if (!kProducerWaitsAcc && !mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err, p.wait_ns)) break;
+                    // the tile to score: the loaded stage, or (MX) its dequantised copy in TMEM
+                    uint64_t* ready = MX ? &ctl->bfull[i & 1] : &ctl->full[s];
+                    if (!mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err, p.wait_ns)) break;
+                    consumed = i + 1;
+                    tc_fence_after();
                     const uint64_t ads = ad0 + (uint64_t)((uint32_t)s * (uint32_t)(Cfg::kStageBytes / 16));
 #pragma unroll
                     for (int k = 0; k < Cfg::kKSteps; ++k) {
@@ -887,14 +899,13 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     if (MX) umma_commit(&ctl->bempty[i & 1]);
                     umma_commit(&ctl->tfull[ab]);
                 }
-                __syncwarp();
-            }
-            if (lane == 0 && !MX) ctl->consumed = consumed;
-            // Drain: tensor memory is released below only once every MMA issued here has completed (the
-            // epilogue has waited for all of them unless a pipeline wait gave up)
-            if (lane == 0 && consumed > 0) {
-                umma_commit(&ctl->mma_done);
-                mbar_wait(&ctl->mma_done, 0, p.err);
+                if (!MX) ctl->consumed = consumed;
+                // Drain: tensor memory is released below only once every MMA issued here has completed (the
+                // epilogue has waited for all of them unless a pipeline wait gave up)
+                if (consumed > 0) {
+                    umma_commit(&ctl->mma_done);
+                    mbar_wait(&ctl->mma_done, 0, p.err);
+                }
             }
             __syncwarp();
         } else if (MX && warp >= 6 && warp < 10) {
