@@ -85,7 +85,9 @@ struct IdxCfg {
 };
 
 constexpr int kCandCap = 256;  // second-round candidates one CTA may send (a power of two)
-constexpr int kRankPick = 256;  // up to this many candidates, the K-th key is found by ranking them directly
+// Up to this many candidates the K-th key is found by ranking them directly (quadratic work); more take two
+// histogram rounds over their low bytes.
+constexpr int kRankPick = 128;
 
 // Words of the per-CTA page list: one per 64-position page, rounded up to whole 16-byte units.
 __host__ __device__ constexpr int page_words(int chunk) { return ((chunk / kPage) + 3) & ~3; }
@@ -530,17 +532,24 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         T = prefix | (b2 << 8) | S.res[2];
     }
     if (fits) {
-        // the candidates above T and equal to it: per CTA, and per warp segment for this CTA's own
-        for (uint32_t c = (uint32_t)tid; c < n_c; c += NT) {
-            uint32_t r = 0, j = c;
-            while (j >= S.ncand_in[r]) j -= S.ncand_in[r++];
-            const uint32_t key = cand[r * kCandCap + j];
-            if (key > T) {
-                atomicAdd(&S.gt[r], 1u);
-                if (r == rank) atomicAdd(&S.scan_s[S.cwarp[j]], 1u);
-            } else if (key == T) {
-                atomicAdd(&S.ecnt[r], 1u);
-                if (r == rank) atomicAdd(&S.scan_e[S.cwarp[j]], 1u);
+        // the candidates above T and equal to it: per CTA (one warp per CTA of the cluster, counted with
+        // ballots), and per warp segment for this CTA's own
+        for (uint32_t r = (uint32_t)warp; r < C; r += (uint32_t)nw) {
+            const uint32_t nr = S.ncand_in[r];
+            uint32_t above = 0, equal = 0;
+            for (uint32_t j = (uint32_t)lane; j < ((nr + 31u) & ~31u); j += 32) {
+                const uint32_t key = j < nr ? cand[r * kCandCap + j] : 0u;
+                const bool a = j < nr && key > T, e = j < nr && key == T;
+                above += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, a));
+                equal += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, e));
+                if (r == rank) {
+                    if (a) atomicAdd(&S.scan_s[S.cwarp[j]], 1u);
+                    if (e) atomicAdd(&S.scan_e[S.cwarp[j]], 1u);
+                }
+            }
+            if (lane == 0) {
+                S.gt[r] += above;
+                S.ecnt[r] += equal;
             }
         }
     } else {
@@ -573,6 +582,8 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     }
     __syncthreads();  // the per-CTA counts (gt, ecnt) and the per-warp counts are complete
     if (tid == 0) {
+        // this CTA's share of the ties (they go to the lowest positions, so to the lowest ranks first) and
+        // its output offset
         uint32_t ties_before = 0, running = 0;
         for (uint32_t r = 0; r < C; ++r) {
             const uint32_t need = remaining > ties_before ? remaining - ties_before : 0u;
@@ -588,14 +599,28 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
     __syncthreads();
     const uint32_t take_me = S.take_me, off_me = S.off_me;
     // Ordered compaction: warp w writes the selected positions of its segment after those of the warps
-    // before it.  Per 128 keys (four per lane), four ballots give each key the number of selected keys
-    // (and ties) in earlier lanes.
-    uint32_t tie_base = 0, out_base = off_me;
-    for (int k = 0; k < warp; ++k) {
-        const uint32_t ties_k = S.scan_e[k];
-        const uint32_t take_k = take_me > tie_base ? min(ties_k, take_me - tie_base) : 0u;
-        out_base += S.scan_s[k] + take_k;
-        tie_base += ties_k;
+    // before it (the same prefix sums over the warps, one lane per warp).  Per 128 keys (four per lane),
+    // ballots give each key the number of selected keys in earlier lanes; only a chunk that holds a key
+    // equal to the K-th key ranks its ties the same way.
+    uint32_t tie_base, out_base;
+    {
+        const uint32_t e = lane < nw ? S.scan_e[lane] : 0u, g = lane < nw ? S.scan_s[lane] : 0u;
+        uint32_t ties_incl = e;
+#pragma unroll
+        for (int off = 1; off < kMaxWarps; off <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, ties_incl, off);
+            if (lane >= off) ties_incl += v;
+        }
+        const uint32_t tb = ties_incl - e;
+        const uint32_t take_k = take_me > tb ? min(e, take_me - tb) : 0u;
+        uint32_t run_incl = g + take_k;
+#pragma unroll
+        for (int off = 1; off < kMaxWarps; off <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, run_incl, off);
+            if (lane >= off) run_incl += v;
+        }
+        tie_base = __shfl_sync(0xFFFFFFFFu, tb, warp);
+        out_base = off_me + __shfl_sync(0xFFFFFFFFu, run_incl - (g + take_k), warp);
     }
     if (S.scan_s[warp] == 0 && (S.scan_e[warp] == 0 || tie_base >= take_me)) return;  // nothing selected here
     const uint32_t lt = lanemask_lt();
@@ -604,23 +629,29 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
         const int i = b0 + 4 * lane;
         const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
         const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
-        uint32_t bt[4], tm = 0;
+        uint32_t tm = 0, sm = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const bool t = kv[e] == T;
-            bt[e] = __ballot_sync(0xFFFFFFFFu, t);
-            tm |= (t ? 1u : 0u) << e;
+            tm |= (kv[e] == T ? 1u : 0u) << e;
+            sm |= (kv[e] > T ? 1u : 0u) << e;
         }
-        uint32_t tie_rank = run_tie;  // ties at earlier positions of this CTA
+        if (__any_sync(0xFFFFFFFFu, tm != 0u)) {
+            // ties in this chunk: rank them among the CTA's ties at earlier positions
+            uint32_t bt[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) tie_rank += (uint32_t)__popc(bt[e] & lt);
-        uint32_t sm = 0;
+            for (int e = 0; e < 4; ++e) bt[e] = __ballot_sync(0xFFFFFFFFu, (tm >> e) & 1u);
+            uint32_t tie_rank = run_tie;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const bool t = (tm >> e) & 1u;
-            const bool sel = kv[e] > T || (t && tie_rank < take_me);
-            tie_rank += t ? 1u : 0u;
-            sm |= (sel ? 1u : 0u) << e;
+            for (int e = 0; e < 4; ++e) tie_rank += (uint32_t)__popc(bt[e] & lt);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if ((tm >> e) & 1u) {
+                    if (tie_rank < take_me) sm |= 1u << e;
+                    ++tie_rank;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) run_tie += (uint32_t)__popc(bt[e]);
         }
         uint32_t bs[4];
 #pragma unroll
@@ -640,10 +671,7 @@ __device__ void cluster_select(const uint32_t* keys, const uint32_t* hist0, uint
             }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            run_tie += (uint32_t)__popc(bt[e]);
-            run_sel += (uint32_t)__popc(bs[e]);
-        }
+        for (int e = 0; e < 4; ++e) run_sel += (uint32_t)__popc(bs[e]);
     }
 }
 
