@@ -61,16 +61,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete.  Gives up after limit_ns, sets
 // DSA_DEVERR_TIMEOUT and returns false; the caller then abandons its pipeline role.  Pipeline waits pass
 // the launch's limit; the drains that must see every issued copy land before shared or tensor memory is
 // reused or released keep the default.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
                                           uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // a non-blocking test first, so that the limit counts from the first look at an incomplete phase (a
+    // first try_wait may already block for a while inside the hardware)
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    // With a limit below the default (failure-detection tests) the wait spins on the non-blocking test, so
+    // that the clock is looked at again within the limit (a try_wait may stay suspended for longer).
+    const bool short_limit = limit_ns < kWaitLimitNs;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) {
             raise_error(err, DSA_DEVERR_TIMEOUT);
             return false;

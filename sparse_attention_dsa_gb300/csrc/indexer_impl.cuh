@@ -791,7 +791,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], MX ? 4 : 1);  // MX: the four converter warps free the stage; else the epilogue
+            mbar_init(&ctl->empty[s], MX ? 4 : 1);  // MX: the four converter warps free the stage; else the MMA commit
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&ctl->tfull[i], 1);
@@ -846,7 +846,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[i % Cfg::kAccBufs], aph ^ 1u, p.err, p.wait_ns)))
                         break;
                 }
-                if (lane == 0) {
+                if (elect_one_sync()) {  // one lane issues, with the warp converged (uniform issue path)
                     const int32_t pg0 = pages_s[2 * i], pg1 = pages_s[2 * i + 1];
                     const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) *
                                            (kPage * Cfg::kRowBytes + Cfg::kScaleStageBytes / 2);
@@ -881,31 +881,33 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
             }
             if (lane == 0) ctl->issued = issued;
         } else if (warp == 1) {
-            // One thread runs the issue loop (lanes 1-31 wait at the warp barrier below): the per-tile cost of
-            // this role is its own instruction stream (a barrier test, a tcgen05 fence, one issue per MMA at
-            // about 46 cycles each, one commit), so no lane votes or warp barriers are added to it.
-            if (lane == 0) {
-                const uint32_t tmem = ctl->tmem_base;
-                int consumed = 0;
-                const bool ok = mbar_wait(&ctl->qbar, 0, p.err, p.wait_ns);
-                ctl->qwaited = ok ? 1 : 0;
-                // Precomputed descriptors: each is a base plus a compile-time offset (the start address field
-                // holds address / 16 and no address here reaches 2^18, so adding to the descriptor adds to the
-                // address).
-                const uint64_t ad0 = smem_desc(smem_u32(a_tiles), 16, 1024, kSwizzle128B);  // stage s: + s * kStageBytes / 16
-                const uint64_t bd0 = smem_desc(smem_u32(q_tile), 16, 1024, kSwizzle128B);
-                int s = 0;
-                uint32_t ph = 0;
-                for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-                    const int ab = i % Cfg::kAccBufs;
-                    const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
-                    // the accumulator buffer is free (seen here, or by the producer before it loaded the stage)
-                    if (!kProducerWaitsAcc && !mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err, p.wait_ns)) break;
-                    // the tile to score: the loaded stage, or (MX) its dequantised copy in TMEM
-                    uint64_t* ready = MX ? &ctl->bfull[i & 1] : &ctl->full[s];
-                    if (!mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err, p.wait_ns)) break;
-                    consumed = i + 1;
-                    tc_fence_after();
+            // The whole warp runs the issue loop and one elected lane issues each tile's MMAs and commit: the
+            // issue path then stays warp-uniform (about 30 cycles per tcgen05.mma, against about 90 from a
+            // single-lane branch, measured on this GPU).  elect.sync picks the lowest lane every time, so the
+            // same thread issues every MMA and the commits that track them.
+            const uint32_t tmem = ctl->tmem_base;
+            int consumed = 0;
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ctl->qbar, 0, p.err, p.wait_ns));
+            if (lane == 0) ctl->qwaited = ok ? 1 : 0;
+            // Precomputed descriptors: each is a base plus a compile-time offset (the start address field holds
+            // address / 16 and no address here reaches 2^18, so adding to the descriptor adds to the address).
+            const uint64_t ad0 = smem_desc(smem_u32(a_tiles), 16, 1024, kSwizzle128B);  // stage s: + s * kStageBytes / 16
+            const uint64_t bd0 = smem_desc(smem_u32(q_tile), 16, 1024, kSwizzle128B);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; ok && i < ntiles; ++i, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+                const int ab = i % Cfg::kAccBufs;
+                const uint32_t aph = (uint32_t)(i / Cfg::kAccBufs) & 1u;
+                // the accumulator buffer is free (seen here, or by the producer before it loaded the stage)
+                if (!kProducerWaitsAcc && !__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tempty[ab], aph ^ 1u, p.err, p.wait_ns)))
+                    break;
+                // the tile to score: the loaded stage, or (MX) its dequantised copy in TMEM
+                uint64_t* ready = MX ? &ctl->bfull[i & 1] : &ctl->full[s];
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(ready, MX ? (((uint32_t)i >> 1) & 1u) : ph, p.err, p.wait_ns)))
+                    break;
+                consumed = i + 1;
+                tc_fence_after();
+                if (elect_one_sync()) {
                     const uint64_t ads = ad0 + (uint64_t)((uint32_t)s * (uint32_t)(Cfg::kStageBytes / 16));
 #pragma unroll
                     for (int k = 0; k < Cfg::kKSteps; ++k) {
@@ -922,18 +924,19 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                         else
                             umma_f8_ss(tmem + ab * Cfg::kN, ad, bd, Cfg::kIdesc, k > 0);
                     }
-                    // MX: the converters free the FP8 stage; otherwise the epilogue frees it once it has seen
-                    // this tile's MMAs complete (one commit per tile for this thread)
-                    if (MX) umma_commit(&ctl->bempty[i & 1]);
+                    // the stage is free once these MMAs complete (MX: the converters free the FP8 stage, and
+                    // this commit frees their TMEM tile); then the accumulator is ready for the epilogue
+                    umma_commit(MX ? &ctl->bempty[i & 1] : &ctl->empty[s]);
                     umma_commit(&ctl->tfull[ab]);
                 }
-                if (!MX) ctl->consumed = consumed;
-                // Drain: tensor memory is released below only once every MMA issued here has completed (the
-                // epilogue has waited for all of them unless a pipeline wait gave up)
-                if (consumed > 0) {
-                    umma_commit(&ctl->mma_done);
-                    mbar_wait(&ctl->mma_done, 0, p.err);
-                }
+                __syncwarp();
+            }
+            if (lane == 0 && !MX) ctl->consumed = consumed;
+            // Drain: tensor memory is released below only once every MMA issued here has completed (the
+            // epilogue has waited for all of them unless a pipeline wait gave up)
+            if (consumed > 0 && elect_one_sync()) {
+                umma_commit(&ctl->mma_done);
+                mbar_wait(&ctl->mma_done, 0, p.err);
             }
             __syncwarp();
         } else if (MX && warp >= 6 && warp < 10) {
@@ -1031,9 +1034,6 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                 float ksc = 1.f;
                 if (FP8 && !MX && pg >= 0) ksc = __ldg(p.k_scale + (int64_t)pg * kPage + (row & 63));
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->tfull[ab], aph, p.err, p.wait_ns))) break;
-                // the tile's MMAs have completed, so its stage is free for the producer (one arrival, from the
-                // first warp of the group that owns the tile)
-                if (!MX && lane == 0 && (warp & 3) == 0 && (!kSplitQueries || group == 0)) mbar_arrive(&ctl->empty[i % S]);
                 tc_fence_after();
                 float acc[QB];
 #pragma unroll
