@@ -539,12 +539,18 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->s_empty);
+            // a row that is not selected (padding, another shard's entry) scores -inf; a tile without one
+            // skips the selects
+            if ((vm0 & vm1) != 0xFFFFFFFFu) {
 #pragma unroll
-            for (int j = 0; j < kRows; ++j) {
-                const uint32_t m = j < 32 ? vm0 : vm1;
-                sv[j] = ((m >> (j & 31)) & 1u) ? sv[j] * p.scale_log2 : -INFINITY;
+                for (int j = 0; j < kRows; ++j) {
+                    const uint32_t m = j < 32 ? vm0 : vm1;
+                    if (!((m >> (j & 31)) & 1u)) sv[j] = -INFINITY;
+                }
             }
-            // row max as a tree (short dependency chains)
+            // row max as a tree (short dependency chains), on the unscaled scores: the scale is positive,
+            // so the scaled maximum is the maximum's scaled value, and the scale joins each exponent's
+            // argument in one fused multiply-add below
             float mx[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) mx[k] = fmaxf(fmaxf(sv[k], sv[k + 16]), fmaxf(sv[k + 32], sv[k + 48]));
@@ -552,7 +558,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
                 for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
-            const float mt = mx[0];
+            const float mt = mx[0] * p.scale_log2;
             const bool raise = mt > m_used + kRescaleLog2;
             const float m_new = raise ? mt : m_used;
             const float alpha = (raise && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
@@ -563,7 +569,8 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < kRows; j += 2) {
-                const uint32_t pk = f2_to_bf2(ex2_approx(sv[j] - mu), ex2_approx(sv[j + 1] - mu));
+                const uint32_t pk = f2_to_bf2(ex2_approx(fmaf(sv[j], p.scale_log2, -mu)),
+                                              ex2_approx(fmaf(sv[j + 1], p.scale_log2, -mu)));
                 packed[j / 2] = pk;
                 // the row sum takes the bf16-rounded values that P V uses
                 ps[(j / 2) & 7] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
