@@ -510,13 +510,23 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
         // ---------------- softmax: one thread per head row ----------------
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t trow = tmem + ((quad * 32u) << 16);
-        for (int i = 0; i < ntiles; ++i) {
-            const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + lane] >= 0);
-            const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rows_s[i * kRows + 32 + lane] >= 0);
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full, (uint32_t)i & 1u, p.err, p.wait_ns))) break;
+        // i = -1 is a dry pass over the loop body (no waits, tensor-memory accesses, state updates or
+        // arrivals) run while the first tile's rows are still in flight: it fetches the body's code, which the
+        // first real pass would otherwise wait for (in the single-launch kernel it follows the indexer phase's
+        // code, and its first pass took several microseconds).
+#pragma unroll 1
+        for (int i = -1; i < ntiles; ++i) {
+            const bool dry = i < 0;
+            const int it = dry ? 0 : i;  // rows_s holds kMaxEntries entries: row 0..63 is always in bounds
+            const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rows_s[it * kRows + lane] >= 0);
+            const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rows_s[it * kRows + 32 + lane] >= 0);
+            if (!dry && !__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->s_full, (uint32_t)i & 1u, p.err, p.wait_ns))) break;
             tc_fence_after();
             float sv[kRows];
-            {
+            if (dry) {
+#pragma unroll
+                for (int j = 0; j < kRows; ++j) sv[j] = 0.f;
+            } else {
                 // all four column groups in flight before one wait
                 float a0[16], a1[16], a2[16], a3[16];
                 tmem_ld16(trow + kSCol, a0);
@@ -536,9 +546,11 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                     sv[48 + j] = a3[j];
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->s_empty);
+            if (!dry) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->s_empty);
+            }
             // a row that is not selected (padding, another shard's entry) scores -inf; a tile without one
             // skips the selects
             if ((vm0 & vm1) != 0xFFFFFFFFu) {
@@ -577,6 +589,10 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
             }
             const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             // P(i-1) V(i-1) has completed: the P columns are free and O is stable
+            if (dry) {
+                asm volatile("" ::"f"(rs));  // the dry pass computes the row sum (so the whole body) for real
+                continue;
+            }
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&ctl->p_empty, ((uint32_t)i & 1u) ^ 1u, p.err, p.wait_ns))) break;
             tc_fence_after();
             if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
