@@ -876,7 +876,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                         }
                     }
                 }
-                __syncwarp();
+                // (no warp barrier here: the next iteration's vote and elect.sync reconverge the warp)
                 issued = i + 1;
             }
             if (lane == 0) ctl->issued = issued;
@@ -929,7 +929,7 @@ __device__ __forceinline__ void indexer_cta(const CUtensorMap& kmap, const CUten
                     umma_commit(MX ? &ctl->bempty[i & 1] : &ctl->empty[s]);
                     umma_commit(&ctl->tfull[ab]);
                 }
-                __syncwarp();
+                // (no warp barrier here: the next iteration's votes and elect.sync reconverge the warp)
             }
             if (lane == 0 && !MX) ctl->consumed = consumed;
             // Drain: tensor memory is released below only once every MMA issued here has completed (the
