@@ -423,8 +423,7 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                     umma_commit(&ctl->v_empty[j & 1]);
                     umma_commit(&ctl->p_empty);
                 }
-                __syncwarp();
-                return true;
+                return true;  // (the next vote or elect.sync reconverges the warp)
             };
             // S += Q atom A . (the part's slot at descriptor bd), K = 64 dims as four MMAs of K = 16 (called
             // by the elected lane)
@@ -472,7 +471,6 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                         qk_atom(K4{}, kd + 4 * kAtomStep, false);
                         umma_commit(&ctl->k_empty[i & 1]);
                     }
-                    __syncwarp();
                     if (i > 0 && !pv(i - 1)) {
                         ok = false;
                         break;
@@ -491,7 +489,6 @@ __device__ __forceinline__ void sfa_cta(const CUtensorMap& qmap, const SfaParams
                         qk_atom(V3{}, vd + 3 * kAtomStep, false);
                         umma_commit(&ctl->s_full);
                     }
-                    __syncwarp();
                 }
             };
             if (dvh == 0)
