@@ -314,8 +314,10 @@ dsa_status_t dsa_clear_device_error(void* workspace, void* stream);
  * up (sets DSA_DEVERR_TIMEOUT, abandons its work, and the kernel still drains its copies in flight and
  * frees its tensor memory under the default limit before it returns).  Applies to launches made after
  * the call, from any host thread; 0 restores the default of one second.  Returns the previous limit.  A
- * short limit makes correct launches report DSA_DEVERR_TIMEOUT (with unspecified outputs): it exists to
- * test that path.  The articles have no counterpart to this call.
+ * wait's clock starts when it first finds its phase incomplete; with a limit below the default, waits
+ * poll instead of suspending, so that the limit is looked at within its own span.  A short limit makes
+ * correct launches report DSA_DEVERR_TIMEOUT (with unspecified outputs): it exists to test that path.
+ * The articles have no counterpart to this call.
  */
 uint64_t dsa_set_wait_limit_ns(uint64_t limit_ns);
 
